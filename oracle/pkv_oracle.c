@@ -1,0 +1,343 @@
+/*
+ * pkv_oracle.c -- plain, slow, fp64 CPU oracle for split-KV paged decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may load, link or call
+ * this file: only the tests, the smoke check and the benchmark's CPU-baseline /
+ * reference leg do.  It shares no code, header, table or constant with the CUDA
+ * library; the two meet only through the seeded input generators.
+ *
+ * What it computes is the plain definition of attention over keys gathered
+ * through a per-request block table, with no splitting, blocking or fusion:
+ * flash-decoding's split-KV decomposition reaches this same result up to the
+ * rounding order, so the definition itself is the oracle.  Every value is
+ * decoded exactly to double and all arithmetic is done in double.
+ *
+ * Sources (page title, then the section the step follows):
+ *  - "vllm.models.flint.ops.decode_attention", flint_decode_attention
+ *    parameters: q [B, num_heads, 128]; kv_cache [num_blocks, num_kv_heads,
+ *    page, 256] with K in [..., :128] and V in [..., 128:]; seq_lens counts the
+ *    KV positions including the current token and 0 writes zeros; window
+ *    attends to the last `window` positions; sinks are per-head fp32 logits.
+ *  - same page, module description ("Numerics ..."): the sink adds
+ *    exp2(sink*log2(e) - m*c) to the final denominator with c = scale*log2(e),
+ *    i.e. exp(sink - scale*m): the sink is a natural-log logit that is NOT
+ *    multiplied by the softmax scale.
+ *  - "vllm.v1.attention.ops.triton_decode_attention", decode_attention_fwd_verify
+ *    parameters: q [B*qlen, H, Lk] with a request's verify tokens contiguous;
+ *    paged latent cache [num_pages, page, 1, Lk]; V is k_buffer[..., :Lv];
+ *    lse is the natural-log LSE, -inf for rows with no key; row limit
+ *    max(min(L - qlen + 1 + t, L_real), 0); k_scale dequantises an FP8 cache.
+ *  - "Atencion paginada" (transformers), decode path: block_table row b holds
+ *    the physical page of each logical page of request b; -1 marks unassigned
+ *    entries; key j of request b lives at page block_table[b][j / page],
+ *    slot j % page.
+ *
+ * Readings taken where the pages are silent:
+ *  - lse excludes the sink (key-only log-sum-exp).  A sink-inclusive value would
+ *    be finite for a row with no key, which the verify page rules out.
+ *  - an MLA row with no key writes zeros, as the GQA path does.
+ *  - window <= 0 means "no window"; otherwise keys [max(L - window, 0), L).
+ *  - FP8 is OCP float8 e4m3 "fn": bias 7, 3 mantissa bits, subnormals,
+ *    no infinities, S.1111.111 is NaN.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG -1
+#define ORACLE_ERR_PAGE -2
+#define ORACLE_ERR_NOMEM -3
+
+/* bfloat16: the upper half of an IEEE-754 binary32 (1 sign, 8 exponent,
+ * 7 stored mantissa bits).  Decoding is exact: place the 16 bits in the high
+ * half of a binary32 and widen. */
+double pkv_oracle_bf16_to_f64(uint16_t bits) {
+    uint32_t w = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* float8 e4m3 (OCP "fn" variant), decoded from the bit fields:
+ *   s eeee mmm, bias 7.  e == 0: subnormal m/8 * 2^-6.  e == 15 and m == 7: NaN.
+ *   otherwise (1 + m/8) * 2^(e - 7).  There is no infinity; max is 448. */
+double pkv_oracle_e4m3_to_f64(uint8_t bits) {
+    int s = (bits >> 7) & 1;
+    int e = (bits >> 3) & 0xF;
+    int m = bits & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* ------------------------------------------------------------------------- */
+/* GQA paged decode                                                           */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    const uint16_t *q;
+    int64_t q_sb, q_sh; /* element strides of q [B, Hq, D], last dim contiguous */
+    const uint16_t *kv;
+    int64_t kv_sblk, kv_sh, kv_stok; /* strides of kv [num_blocks, Hkv, P, 2D] */
+    int64_t num_blocks;
+    const int32_t *bt;
+    int64_t bt_sb, max_blocks;
+    const int32_t *seq_lens;
+    const float *sinks; /* [Hq] or NULL */
+    int window;
+    double scale;
+    int page_size, B, Hq, Hkv, D;
+    const int64_t *rows; /* row = b * Hq + h; NULL means all B*Hq rows */
+    int64_t nrows;
+    double *out; /* [nrows, D] */
+    double *lse; /* [nrows] */
+    int status;
+} gqa_job;
+
+/* One output row of GQA decode: query head h of request b against kv head
+ * h / (Hq / Hkv), over keys [s, L) gathered through the block table. */
+static int gqa_row(const gqa_job *a, int64_t row, double *out, double *lse) {
+    const int D = a->D, P = a->page_size;
+    const int b = (int)(row / a->Hq), h = (int)(row % a->Hq);
+    const int g = h / (a->Hq / a->Hkv);
+    const int L = a->seq_lens[b];
+    int s = 0;
+    if (a->window > 0 && L > a->window) s = L - a->window;
+    const int n = L > s ? L - s : 0;
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    if (n == 0) {
+        *lse = -INFINITY;
+        return ORACLE_OK;
+    }
+    if ((int64_t)((L + P - 1) / P) > a->max_blocks) return ORACLE_ERR_PAGE;
+
+    double *x = (double *)malloc(sizeof(double) * (size_t)n);
+    double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+    const uint16_t **vrow = (const uint16_t **)malloc(sizeof(uint16_t *) * (size_t)n);
+    if (!x || !qd || !vrow) {
+        free(x); free(qd); free(vrow);
+        return ORACLE_ERR_NOMEM;
+    }
+    const uint16_t *qrow = a->q + (int64_t)b * a->q_sb + (int64_t)h * a->q_sh;
+    for (int d = 0; d < D; ++d) qd[d] = pkv_oracle_bf16_to_f64(qrow[d]);
+
+    /* gather + scores */
+    for (int j = s; j < L; ++j) {
+        const int32_t page = a->bt[(int64_t)b * a->bt_sb + j / P];
+        const int slot = j % P;
+        if (page < 0 || (int64_t)page >= a->num_blocks) {
+            free(x); free(qd); free(vrow);
+            return ORACLE_ERR_PAGE;
+        }
+        const uint16_t *krow = a->kv + (int64_t)page * a->kv_sblk +
+                               (int64_t)g * a->kv_sh + (int64_t)slot * a->kv_stok;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += qd[d] * pkv_oracle_bf16_to_f64(krow[d]);
+        x[j - s] = a->scale * dot;
+        vrow[j - s] = krow + D; /* V occupies [..., D:2D] of the same token row */
+    }
+    /* dense softmax */
+    double M = -INFINITY;
+    for (int i = 0; i < n; ++i)
+        if (x[i] > M) M = x[i];
+    double Z = 0.0;
+    for (int i = 0; i < n; ++i) Z += exp(x[i] - M);
+    double den = Z;
+    if (a->sinks) den += exp((double)a->sinks[h] - M);
+    for (int i = 0; i < n; ++i) {
+        const double w = exp(x[i] - M) / den;
+        for (int d = 0; d < D; ++d) out[d] += w * pkv_oracle_bf16_to_f64(vrow[i][d]);
+    }
+    *lse = M + log(Z);
+    free(x); free(qd); free(vrow);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* MLA causal verify                                                          */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    const uint16_t *q;
+    int64_t q_sr, q_sh; /* strides of q [B*qlen, H, Lk] */
+    const uint8_t *cache; /* bf16 (2 bytes) or e4m3 (1 byte) elements */
+    int fp8;
+    int64_t c_spage, c_stok; /* element strides of the cache [num_pages, P, 1, Lk] */
+    int64_t num_pages;
+    const int32_t *bt;
+    int64_t bt_sb, max_blocks;
+    const int32_t *seq_lens, *real_seq_lens; /* real may be NULL */
+    int qlen;
+    double scale, k_scale;
+    int page_size, B, H, Lk, Lv;
+    const int64_t *rows; /* row = r * H + h, r = b * qlen + t */
+    int64_t nrows;
+    double *out; /* [nrows, Lv] */
+    double *lse;
+    int status;
+} mla_job;
+
+static double cache_elem(const mla_job *a, int64_t idx) {
+    if (a->fp8) return pkv_oracle_e4m3_to_f64(a->cache[idx]) * a->k_scale;
+    uint16_t bits;
+    memcpy(&bits, a->cache + 2 * idx, 2);
+    return pkv_oracle_bf16_to_f64(bits);
+}
+
+/* One output row of MLA verify: head h of verify token t of request b, over
+ * keys [0, lim) with lim = max(min(L - qlen + 1 + t, L_real), 0).  The single
+ * latent head serves every query head; V is the first Lv dims of K. */
+static int mla_row(const mla_job *a, int64_t row, double *out, double *lse) {
+    const int Lk = a->Lk, Lv = a->Lv, P = a->page_size;
+    const int64_t r = row / a->H;
+    const int h = (int)(row % a->H);
+    const int b = (int)(r / a->qlen), t = (int)(r % a->qlen);
+    const int L = a->seq_lens[b];
+    const int Lr = a->real_seq_lens ? a->real_seq_lens[b] : L;
+    int lim = L - a->qlen + 1 + t;
+    if (Lr < lim) lim = Lr;
+    if (lim < 0) lim = 0;
+    for (int d = 0; d < Lv; ++d) out[d] = 0.0;
+    if (lim == 0) {
+        *lse = -INFINITY;
+        return ORACLE_OK;
+    }
+    if ((int64_t)((lim + P - 1) / P) > a->max_blocks) return ORACLE_ERR_PAGE;
+
+    double *x = (double *)malloc(sizeof(double) * (size_t)lim);
+    double *qd = (double *)malloc(sizeof(double) * (size_t)Lk);
+    int64_t *kbase = (int64_t *)malloc(sizeof(int64_t) * (size_t)lim);
+    if (!x || !qd || !kbase) {
+        free(x); free(qd); free(kbase);
+        return ORACLE_ERR_NOMEM;
+    }
+    const uint16_t *qrow = a->q + r * a->q_sr + (int64_t)h * a->q_sh;
+    for (int d = 0; d < Lk; ++d) qd[d] = pkv_oracle_bf16_to_f64(qrow[d]);
+    for (int j = 0; j < lim; ++j) {
+        const int32_t page = a->bt[(int64_t)b * a->bt_sb + j / P];
+        if (page < 0 || (int64_t)page >= a->num_pages) {
+            free(x); free(qd); free(kbase);
+            return ORACLE_ERR_PAGE;
+        }
+        kbase[j] = (int64_t)page * a->c_spage + (int64_t)(j % P) * a->c_stok;
+        double dot = 0.0;
+        for (int d = 0; d < Lk; ++d) dot += qd[d] * cache_elem(a, kbase[j] + d);
+        x[j] = a->scale * dot;
+    }
+    double M = -INFINITY;
+    for (int j = 0; j < lim; ++j)
+        if (x[j] > M) M = x[j];
+    double Z = 0.0;
+    for (int j = 0; j < lim; ++j) Z += exp(x[j] - M);
+    for (int j = 0; j < lim; ++j) {
+        const double w = exp(x[j] - M) / Z;
+        for (int d = 0; d < Lv; ++d) out[d] += w * cache_elem(a, kbase[j] + d);
+    }
+    *lse = M + log(Z);
+    free(x); free(qd); free(kbase);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Row-parallel driver: threads only split the independent output rows.       */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    void *job;
+    int kind; /* 0 = gqa, 1 = mla */
+    int64_t next;
+    pthread_mutex_t mu;
+    int status;
+} pool_t;
+
+static void *worker(void *arg) {
+    pool_t *p = (pool_t *)arg;
+    for (;;) {
+        pthread_mutex_lock(&p->mu);
+        const int64_t i = p->next++;
+        pthread_mutex_unlock(&p->mu);
+        int rc;
+        if (p->kind == 0) {
+            gqa_job *a = (gqa_job *)p->job;
+            if (i >= a->nrows) break;
+            const int64_t row = a->rows ? a->rows[i] : i;
+            rc = gqa_row(a, row, a->out + i * a->D, a->lse + i);
+        } else {
+            mla_job *a = (mla_job *)p->job;
+            if (i >= a->nrows) break;
+            const int64_t row = a->rows ? a->rows[i] : i;
+            rc = mla_row(a, row, a->out + i * a->Lv, a->lse + i);
+        }
+        if (rc != ORACLE_OK) {
+            pthread_mutex_lock(&p->mu);
+            if (p->status == ORACLE_OK) p->status = rc;
+            pthread_mutex_unlock(&p->mu);
+        }
+    }
+    return NULL;
+}
+
+static int run_pool(void *job, int kind, int nthreads) {
+    pool_t p;
+    p.job = job;
+    p.kind = kind;
+    p.next = 0;
+    p.status = ORACLE_OK;
+    pthread_mutex_init(&p.mu, NULL);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 512) nthreads = 512;
+    pthread_t th[512];
+    int started = 0;
+    for (int i = 1; i < nthreads; ++i)
+        if (pthread_create(&th[started], NULL, worker, &p) == 0) ++started;
+    worker(&p);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    pthread_mutex_destroy(&p.mu);
+    return p.status;
+}
+
+int pkv_oracle_gqa_decode(const uint16_t *q, int64_t q_sb, int64_t q_sh,
+                          const uint16_t *kv, int64_t kv_sblk, int64_t kv_sh,
+                          int64_t kv_stok, int64_t num_blocks, const int32_t *bt,
+                          int64_t bt_sb, int64_t max_blocks, const int32_t *seq_lens,
+                          const float *sinks, int window, double scale, int page_size,
+                          int B, int Hq, int Hkv, int D, const int64_t *rows,
+                          int64_t nrows, double *out, double *lse, int nthreads) {
+    if (!q || !kv || !bt || !seq_lens || !out || !lse) return ORACLE_ERR_ARG;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || page_size <= 0)
+        return ORACLE_ERR_ARG;
+    if (!rows) nrows = (int64_t)B * Hq;
+    for (int64_t i = 0; rows && i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= (int64_t)B * Hq) return ORACLE_ERR_ARG;
+    gqa_job a = {q, q_sb, q_sh, kv, kv_sblk, kv_sh, kv_stok, num_blocks, bt, bt_sb,
+                 max_blocks, seq_lens, sinks, window, scale, page_size, B, Hq, Hkv, D,
+                 rows, nrows, out, lse, ORACLE_OK};
+    return run_pool(&a, 0, nthreads);
+}
+
+int pkv_oracle_mla_verify(const uint16_t *q, int64_t q_sr, int64_t q_sh,
+                          const void *cache, int fp8, int64_t c_spage, int64_t c_stok,
+                          int64_t num_pages, const int32_t *bt, int64_t bt_sb,
+                          int64_t max_blocks, const int32_t *seq_lens,
+                          const int32_t *real_seq_lens, int qlen, double scale,
+                          int page_size, double k_scale, int B, int H, int Lk, int Lv,
+                          const int64_t *rows, int64_t nrows, double *out, double *lse,
+                          int nthreads) {
+    if (!q || !cache || !bt || !seq_lens || !out || !lse) return ORACLE_ERR_ARG;
+    if (B < 0 || H <= 0 || qlen <= 0 || Lk <= 0 || Lv <= 0 || Lv > Lk || page_size <= 0)
+        return ORACLE_ERR_ARG;
+    if (!rows) nrows = (int64_t)B * qlen * H;
+    for (int64_t i = 0; rows && i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= (int64_t)B * qlen * H) return ORACLE_ERR_ARG;
+    mla_job a = {q, q_sr, q_sh, (const uint8_t *)cache, fp8, c_spage, c_stok, num_pages,
+                 bt, bt_sb, max_blocks, seq_lens, real_seq_lens, qlen, scale, k_scale,
+                 page_size, B, H, Lk, Lv, rows, nrows, out, lse, ORACLE_OK};
+    return run_pool(&a, 1, nthreads);
+}
