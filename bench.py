@@ -1,0 +1,425 @@
+#!/usr/bin/env python3
+"""Benchmark: split-KV paged GQA decode attention on GB300.
+
+One step = one pass of the decode attention hot path over one batch of the
+Flint-shaped workload: B=64 requests, Hq=64, Hkv=8, head_dim 128, bf16 HND
+pages of 16 tokens, log-uniform lengths in [1, 32768], per-head sinks, and the
+workload's two layer types -- a full-attention layer and a sliding-window
+(128) layer, each with its own KV cache -- so two library calls per step.
+
+Prints one JSON line (rank 0).  `value` is KV-cache GB/s over the step
+(algorithmic bytes: attended tokens x Hkv x 512 B) with inputs resident in HBM
+and L2 flushed between steps; `e2e` repeats the measurement through the same C
+ABI call with the step's inputs copied from pinned host memory and the
+outputs copied back inside the timed region.  `roofline` covers the dominant
+kernel (the full-attention layer) against the measured HBM copy bandwidth.
+`cpu_baseline` is the fp64 CPU oracle timed on this host on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV-cache read GB/s (% of GB300 HBM peak) and attention calls/sec at 1 GPU"
+UNIT = "GB/s"
+WORKLOAD = ("flint_gqa_b64: B=64, Hq=64, Hkv=8, head_dim=128, bf16 HND pages of 16 tokens, "
+            "seq_lens log-uniform in [1,32768], random block tables, fp32 sinks; one "
+            "full-attention layer + one sliding-window-128 layer per step")
+FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
+KERNEL_SOURCES = ["paged_kv_cache_30_gb300/csrc/gqa_decode.cu",
+                  "paged_kv_cache_30_gb300/csrc/ptx.cuh",
+                  "paged_kv_cache_30_gb300/csrc/pkv_internal.h"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the full-layer kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "gqa_decode_flint_b64_full.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("kernel_hash") == kernel_hash():
+            return d.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------- clocks ----
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        def reader():
+            for line in self.proc.stdout:
+                self.lines.append((time.time(), line.strip()))
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15]
+        if not inside and rows:
+            inside = [min(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[2]) for _, p in inside if num(p[2]) is not None]
+        mx = [num(p[3]) for _, p in inside if num(p[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in inside for i in range(4)
+                          if p[6 + i].lower().startswith("active")})
+        pw = [num(p[4]) for _, p in inside if num(p[4]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------ workload ----
+def make_layers(seed: int):
+    """The step's batch: one set of requests (lengths, block tables) and two
+    layers, each with its own KV cache, queries and sinks."""
+    from paged_kv_cache_30_gb300 import workloads as W
+    full = W.flint_gqa(seed, window=0)
+    slide = W.GQAProblem(
+        q=W.normal(full.q.shape, seed * 7919 + 101),
+        kv_cache=W.normal(full.kv_cache.shape, seed * 7919 + 102),
+        block_table=full.block_table, seq_lens=full.seq_lens,
+        sinks=W.normal(full.sinks.shape, seed * 7919 + 103, dtype=full.sinks.dtype),
+        window=128, scale=full.scale, page_size=16, name="flint_gqa_b64_w128")
+    return [full, slide]
+
+
+def oracle_baseline(layers, budget_s: float, threads: int):
+    """Time the fp64 oracle on a bounded sample: whole (request, kv head)
+    groups of the full layer, taken round-robin, until ~budget_s of work."""
+    import numpy as np
+    import oracle
+    full = layers[0]
+    B, Hq, _ = full.q.shape
+    Hkv = full.kv_cache.shape[1]
+    L = full.seq_lens.numpy().astype(np.int64)
+    order = np.argsort(-L)  # longest first: representative bytes per second
+    done_bytes, t_used, groups = 0, 0.0, 0
+    i = 0
+    while t_used < budget_s and i < B * Hkv:
+        b = int(order[(i // Hkv) % B])
+        kvh = i % Hkv
+        rows = np.arange(b * Hq + kvh * 8, b * Hq + kvh * 8 + 8, dtype=np.int64)
+        t = time.perf_counter()
+        oracle.gqa_decode(full.q, full.kv_cache, full.block_table, full.seq_lens, full.sinks, 0,
+                          full.scale, 16, rows=rows, nthreads=threads)
+        t_used += time.perf_counter() - t
+        done_bytes += int(L[b]) * 512
+        groups += 1
+        i += 1
+    return done_bytes / t_used / 1e9, t_used, groups
+
+
+# ------------------------------------------------------------- reference ---
+def run_reference(args, rank, world):
+    """The oracle, as it stands, on the host cores: same workload, metric and
+    unit; each step a bounded sample (whole kv-head groups of the full layer)."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    oracle.build()
+    layers = make_layers(args.seed)
+    full = layers[0]
+    B, Hq, _ = full.q.shape
+    Hkv = full.kv_cache.shape[1]
+    L = full.seq_lens.numpy().astype(np.int64)
+    threads = os.cpu_count() or 1
+    total_steps = args.steps + args.warmup
+    per_step = min(4.0, 150.0 / max(1, total_steps))
+    rng = np.random.default_rng(args.seed)
+    cand = [(b, k) for b in range(B) for k in range(Hkv)]
+
+    def one_step():
+        t0 = time.perf_counter()
+        nbytes = 0
+        while True:
+            b, kvh = cand[int(rng.integers(len(cand)))]
+            rows = np.arange(b * Hq + kvh * 8, b * Hq + kvh * 8 + 8, dtype=np.int64)
+            oracle.gqa_decode(full.q, full.kv_cache, full.block_table, full.seq_lens,
+                              full.sinks, 0, full.scale, 16, rows=rows, nthreads=threads)
+            nbytes += int(L[b]) * 512
+            if time.perf_counter() - t0 >= per_step:
+                return nbytes, time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        one_step()
+    tot_b, tot_t = 0, 0.0
+    for _ in range(args.steps):
+        nb, dt = one_step()
+        tot_b += nb
+        tot_t += dt
+    value = tot_b / tot_t / 1e9
+    sample = (f"random (request, kv head) groups of the full-attention layer, all 8 query "
+              f"heads each, ~{per_step:.2f} s of oracle work per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 64, "seed": args.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- main arm --
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import paged_kv_cache_30_gb300 as pkv
+    from paged_kv_cache_30_gb300 import build as pkv_build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a GPU")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pkv_build.build()
+    pkv.load_library()
+    pkv.init(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    # weak scaling: every rank runs its own batch of 64 requests
+    layers = make_layers(args.seed + 7919 * rank)
+    kv_bytes = [p.kv_bytes() for p in layers]
+    step_bytes = sum(kv_bytes)
+    stream = torch.cuda.current_stream(dev)
+    d = []
+    bt_dev = layers[0].block_table.to(dev)
+    sl_dev = layers[0].seq_lens.to(dev)
+    for p in layers:
+        d.append(dict(q=p.q.to(dev), kv=p.kv_cache.to(dev), bt=bt_dev, sl=sl_dev,
+                      sinks=p.sinks.to(dev), out=torch.empty_like(p.q, device=dev),
+                      lse=torch.empty(p.q.shape[:2], device=dev)))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def call(i):
+        p, t = layers[i], d[i]
+        pkv.paged_decode_attn(t["q"], t["kv"], t["bt"], t["sl"], t["sinks"], p.window, p.scale,
+                              16, 0, t["out"], t["lse"])
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---------------- device-resident timing ----------------
+    for _ in range(args.warmup):
+        call(0); call(1)
+        flush.fill_(1.0)
+    assert pkv.check_errors(local_rank) == 0
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    t0 = time.time()
+    for s in range(args.steps):
+        e = ev[s]
+        e[0].record(stream)
+        call(0)
+        e[1].record(stream)
+        call(1)
+        e[2].record(stream)
+        flush.fill_(float(s & 7))  # outside the events: evicts L2 between steps
+    barrier()
+    t1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    full_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    step_ms = [ev[s][0].elapsed_time(ev[s][2]) for s in range(args.steps)]
+    total_ms = sum(step_ms)
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    calls_per_s = world * 2 / (ms_per_step * 1e-3)
+    full_mean = statistics.mean(full_ms)
+    achieved = kv_bytes[0] / (full_mean * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    assert pkv.check_errors(local_rank) == 0
+
+    # ---------------- end to end through the same call, host buffers ----------------
+    hq = [p.q.pin_memory() for p in layers]
+    hbt = layers[0].block_table.pin_memory()
+    hsl = layers[0].seq_lens.pin_memory()
+    hout = [torch.empty(p.q.shape, dtype=torch.bfloat16).pin_memory() for p in layers]
+    hlse = [torch.empty(p.q.shape[:2], dtype=torch.float32).pin_memory() for p in layers]
+    h2d = sum(x.numel() * x.element_size() for x in hq) + hbt.numel() * 4 + hsl.numel() * 4
+    d2h = sum(x.numel() * x.element_size() for x in hout) + sum(x.numel() * 4 for x in hlse)
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    barrier()
+    for s in range(args.steps):
+        e2e_ev[s][0].record(stream)
+        for i in range(2):
+            d[i]["q"].copy_(hq[i], non_blocking=True)
+        bt_dev.copy_(hbt, non_blocking=True)
+        sl_dev.copy_(hsl, non_blocking=True)
+        call(0)
+        call(1)
+        for i in range(2):
+            hout[i].copy_(d[i]["out"], non_blocking=True)
+            hlse[i].copy_(d[i]["lse"], non_blocking=True)
+        e2e_ev[s][1].record(stream)
+        flush.fill_(float(s & 7))
+    barrier()
+    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in e2e_ev)
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * step_bytes / (e2e_ms / args.steps * 1e-3) / 1e9
+    assert pkv.check_errors(local_rank) == 0
+
+    if dist:
+        dist.barrier()
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    # ---------------- CPU baseline: the oracle on this host ----------------
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        threads = os.cpu_count() or 1
+        v, t_used, groups = oracle_baseline(layers, args.cpu_budget, threads)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{groups} (request, kv head) groups of the full-attention layer "
+                         f"(longest requests first, all 8 query heads each), "
+                         f"{t_used:.1f} s of fp64 oracle work on {threads} threads"}
+
+    clocks = sampler.summary(t0, t1)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 64 * world, "seed": args.seed,
+                   "kv_bytes_per_step": step_bytes, "kv_bytes_full_layer": kv_bytes[0],
+                   "l2": "flushed between steps (512 MiB write outside the timed events)",
+                   "parallelism": f"{world} independent ranks" if world > 1 else "single GPU"},
+        "calls_per_s": calls_per_s,
+        "hbm_frac_of_measured": value / peak,
+        "hbm_frac_of_nominal_8tbs": value / 8000.0,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(),
+                     "kernel": "gqa_decode_kernel<16> (full-attention layer)",
+                     "peak_source": f"{peak_kind} hbm_gbs", "launch_ms": full_mean},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "kernel_hash": kernel_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and world > 1:
+        print(f"warning: WORLD_SIZE={world} but --gpus {args.gpus}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

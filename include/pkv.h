@@ -1,0 +1,225 @@
+/*
+ * pkv.h -- C ABI of libpkv: split-KV paged decode attention on GB300 (sm_103a).
+ *
+ * Two operations, each one kernel launch on the caller's stream:
+ *
+ *  - pkv_paged_decode_attn: GQA decode.  Every request has one query token per
+ *    query head; it attends to the keys of its KV cache, gathered page by page
+ *    through a per-request block table, optionally restricted to a sliding
+ *    window and with a per-head attention sink in the softmax denominator.
+ *    Defined by "vllm.models.flint.ops.decode_attention" (flint_decode_attention:
+ *    parameters and the module's numerics paragraph) and, for the block table,
+ *    by the transformers page "Atencion paginada" (decode path).
+ *
+ *  - pkv_mla_verify_attn: MLA causal verify.  qlen consecutive verify tokens of
+ *    a request, 128 query heads each, attend to one shared 576-wide latent head;
+ *    V is the first 512 dims of the latent K; verify token t sees
+ *    max(min(L - qlen + 1 + t, L_real), 0) keys.  The latent cache is bf16 or
+ *    FP8 e4m3 with a scalar dequantisation factor.  Defined by
+ *    "vllm.v1.attention.ops.triton_decode_attention"
+ *    (decode_attention_fwd_verify: parameters).
+ *
+ * Both compute the fp32 online softmax of the pages (exp2 with the softmax
+ * scale folded into log2(e), P rounded to bf16 for P.V, fp32 accumulation),
+ * split each request's keys over several CTAs, and merge the fp32
+ * (unnormalised O, running max m, sum l) partials of the splits into a bf16
+ * output and a natural-log LSE that is -inf for rows with no key.
+ *
+ * Conventions shared by every entry point
+ *  - Return value: PKV_OK (0) or a negative PKV_ERR_* code.  No call aborts
+ *    the process.  The message of the last failure on the calling thread is
+ *    returned by pkv_last_error().
+ *  - Tensors are caller-owned device memory described by pkv_tensor (shape and
+ *    strides in elements).  The library never frees caller memory.  It owns
+ *    only its per-device workspace (split partials, arrival counters,
+ *    scheduler words, error word), allocated once by pkv_init() or by the
+ *    first call on a device, and never moved afterwards, so launches captured
+ *    in a CUDA graph keep valid pointers.
+ *  - Calls that share a device's workspace must be ordered on one stream (as
+ *    within one model forward).  When a call arrives on a different stream
+ *    than the previous call on that device (and neither is being captured),
+ *    the new stream first waits for the previous one.
+ *  - The launch shape depends only on the device and the batch size, never on
+ *    the sequence lengths or the block table, which the kernels read on the
+ *    device: a captured graph stays valid when seq_lens and block_table change.
+ *  - Data-dependent input errors that the host cannot see (a block-table entry
+ *    outside the cache, a seq_len longer than the block table) never fault:
+ *    the kernel clamps or zero-fills, raises a bit in the device error word and
+ *    finishes; pkv_check_errors() reads and clears that word.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_API __attribute__((visibility("default")))
+
+/* Status codes. */
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG -1     /* NULL pointer, bad shape, dtype or value */
+#define PKV_ERR_UNSUPPORTED -2     /* valid but not built: head dim, page size, group size, batch */
+#define PKV_ERR_ALIGNMENT -3       /* pointer or stride breaks a 16-byte rule */
+#define PKV_ERR_WORKSPACE -4       /* the workspace cannot hold this call's split partials */
+#define PKV_ERR_CAPTURE -5         /* workspace first needed while the stream is being captured */
+#define PKV_ERR_CUDA -6            /* a CUDA runtime or driver call failed (see pkv_last_error) */
+#define PKV_ERR_BAD_BLOCK_TABLE -7 /* reported by pkv_check_errors for bad block-table data */
+
+/* Element types of pkv_tensor. */
+#define PKV_DTYPE_BF16 1
+#define PKV_DTYPE_F32 2
+#define PKV_DTYPE_I32 3
+#define PKV_DTYPE_FP8_E4M3 4 /* OCP float8 e4m3 ("fn": no infinities) */
+
+/* A strided view of caller-owned device memory. */
+typedef struct pkv_tensor {
+  void* data;        /* device pointer */
+  int32_t dtype;     /* PKV_DTYPE_* */
+  int32_t ndim;      /* 0..5 (0 = scalar) */
+  int64_t shape[5];  /* sizes of the first ndim dimensions */
+  int64_t stride[5]; /* strides in elements */
+} pkv_tensor;
+
+/*
+ * pkv_init -- allocate the workspace of `device` once (idempotent).
+ *   workspace_bytes: bytes for split partials; 0 selects the default
+ *   (1 GiB).  The first call on a device fixes the size; later calls are
+ *   no-ops that return PKV_OK.  Also zeroes the arrival counters and the
+ *   scheduler words, which the kernels keep at zero between calls.
+ *   Errors: PKV_ERR_CAPTURE when called while the current stream of the
+ *   device is capturing, PKV_ERR_CUDA when allocation fails.
+ *   Source: "vllm.models.flint.ops.decode_attention", _workspace (persistent
+ *   partials and counters allocated once per device at a fixed maximum,
+ *   never replaced; counters zeroed only at allocation).
+ */
+PKV_API int pkv_init(int device, size_t workspace_bytes);
+
+/*
+ * pkv_paged_decode_attn -- GQA paged decode attention with sinks, one query
+ * token per request.
+ * Source: "vllm.models.flint.ops.decode_attention", flint_decode_attention
+ * (parameters; numerics paragraph of the module; _launch_config /
+ * _supports_kv_cache for the layout rules).
+ *
+ *   q            bf16 [B, Hq, 128]; last dim contiguous; strides multiples of 8;
+ *                16-byte aligned.
+ *   kv_cache     bf16 [num_blocks, Hkv, P, 256] HND pages: K in [..., :128],
+ *                V in [..., 128:]; stride(3) == 1, stride(2) == 256,
+ *                stride(0) and stride(1) multiples of 8; 16-byte aligned.
+ *                Hq == 8 * Hkv: query head h reads kv head h / 8.
+ *   block_table  int32 [B, max_blocks]; row b lists the physical block of
+ *                each logical page of request b; entries past the request's
+ *                last page (and before its window) are never read and may be
+ *                -1.  stride(1) == 1.
+ *   seq_lens     int32 [B]: attended positions of request b including the
+ *                current token (keys [0, L)); 0 writes zeros and lse = -inf.
+ *   sinks        fp32 [Hq] natural-log sink logits (not multiplied by scale),
+ *                or NULL for none.  They enter only the output's denominator;
+ *                lse is over the keys alone.
+ *   window       > 0: attend to keys [max(L - window, 0), L); <= 0: all keys.
+ *   scale        softmax scale applied to q.k.
+ *   page_size    P, tokens per page: 16 or 32 (must equal kv_cache.shape[2]).
+ *   num_kv_splits static cap on the number of KV splits of one (request, kv
+ *                head); 0 selects the library's cap.  Each request uses as
+ *                many splits as its own length warrants, at most this many.
+ *   out          bf16 [B, Hq, 128] (may not alias q); last dim contiguous.
+ *   lse          fp32 [B, Hq] or NULL.
+ *   stream       cudaStream_t (NULL = legacy default stream).
+ * B == 0 returns PKV_OK without launching.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED (head dim != 128, Hq != 8*Hkv,
+ * P not in {16, 32}, B > 2048), PKV_ERR_ALIGNMENT, PKV_ERR_WORKSPACE (B * Hkv *
+ * cap partials do not fit), PKV_ERR_CAPTURE, PKV_ERR_CUDA.
+ */
+PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cache,
+                                  const pkv_tensor* block_table, const pkv_tensor* seq_lens,
+                                  const pkv_tensor* sinks, int window, float scale,
+                                  int page_size, int num_kv_splits, const pkv_tensor* out,
+                                  const pkv_tensor* lse, void* stream);
+
+/*
+ * pkv_mla_verify_attn -- causal MLA verify over a per-request block table.
+ * Source: "vllm.v1.attention.ops.triton_decode_attention",
+ * decode_attention_fwd_verify (parameters).
+ *
+ *   q             bf16 [B*qlen, H, 576], a request's verify tokens contiguous;
+ *                 last dim contiguous; 16-byte aligned rows.
+ *   latent_cache  bf16 or FP8 e4m3 [num_pages, P, 1, 576] (or
+ *                 [num_pages*P, 1, 576]); one latent head; last dim contiguous;
+ *                 pages 16-byte aligned.  V is latent[..., :512].
+ *   block_table   int32 [B, max_pages].
+ *   seq_lens      int32 [B], kernel KV lengths L.
+ *   real_seq_lens int32 [B] or NULL (= seq_lens).  Verify token t of request b
+ *                 attends to keys [0, max(min(L - qlen + 1 + t, L_real), 0)).
+ *   qlen          verify tokens per request (>= 1).
+ *   scale         softmax scale.
+ *   page_size     P, tokens per page (16 or 32).
+ *   k_scale       fp32 device scalar (ndim 0 or 1 element) dequantising an FP8
+ *                 cache, or NULL (= 1); ignored for a bf16 cache.
+ *   out           bf16 [B*qlen, H, 512].
+ *   lse           fp32 [B*qlen, H]; -inf for rows with no key (their out is 0).
+ *   num_kv_splits static cap on KV splits per request, 0 = the library's choice
+ *                 (an addition to the page's list: the workspace the page passes
+ *                 as attn_logits is owned by the library here).
+ *   stream        cudaStream_t.
+ * Errors: as pkv_paged_decode_attn; PKV_ERR_UNSUPPORTED unless Lk == 576,
+ * Lv == 512 and H == 128.
+ */
+PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_cache,
+                                const pkv_tensor* block_table, const pkv_tensor* seq_lens,
+                                const pkv_tensor* real_seq_lens, int qlen, float scale,
+                                int page_size, const pkv_tensor* k_scale, const pkv_tensor* out,
+                                const pkv_tensor* lse, int num_kv_splits, void* stream);
+
+/*
+ * pkv_num_kv_splits -- static upper bound on KV splits, safe to bake into a
+ * CUDA graph (host only, no GPU needed).
+ * Source: "vllm.v1.attention.ops.triton_decode_attention", verify_num_kv_splits
+ * (its contract: programs per split = batch x row blocks; if one split of
+ * every request fits in one dispatch round of occupancy x sm_count slots, use
+ * as many splits as fit; else the n <= max_splits minimising rounds(n)/n,
+ * preferring the fewest splits within 5 % of the best; never more than
+ * cdiv(max_seq_len, min_work_per_split) nor 2 x sm_count, never fewer than 1).
+ *   row blocks = cdiv(qlen * num_heads, block_h).
+ * Returns the cap (>= 1), or PKV_ERR_INVALID_ARG for non-positive sm_count,
+ * block_h, qlen or num_heads, or a negative occupancy.
+ */
+PKV_API int pkv_num_kv_splits(int max_seq_len, int batch, int qlen, int num_heads, int sm_count,
+                              int block_h, double occupancy, int min_work_per_split,
+                              int max_splits);
+
+/*
+ * pkv_check_errors -- read and clear the device error word of `device`
+ * (synchronises the device).  *flags receives the OR of the bits raised since
+ * the last check: 1 bad block-table entry, 2 seq_len longer than the block
+ * table, 4 a pipeline wait gave up, 8 work items beyond the workspace.
+ * Returns PKV_OK when no bit was set, PKV_ERR_BAD_BLOCK_TABLE for bits 1|2,
+ * PKV_ERR_CUDA otherwise (or on a failed CUDA call).
+ */
+PKV_API int pkv_check_errors(int device, int32_t* flags);
+
+/*
+ * pkv_check_counters -- count the non-zero arrival counters and scheduler
+ * words of `device` (synchronises the device).  The kernels reset every
+ * counter they use before returning, so a non-zero count after a completed
+ * call means a broken invariant.  *nonzero receives the count.
+ */
+PKV_API int pkv_check_counters(int device, int64_t* nonzero);
+
+/* Message of the last failed call on this thread ("" if none). */
+PKV_API const char* pkv_last_error(void);
+
+/* Free every device's workspace.  Later calls allocate afresh. */
+PKV_API int pkv_shutdown(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+PKV_API int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

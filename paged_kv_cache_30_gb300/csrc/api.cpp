@@ -1,0 +1,470 @@
+// api.cpp -- the C ABI of libpkv (see include/pkv.h): argument validation,
+// per-device workspace, tensor-map encoding, the static split-cap heuristic
+// and kernel launches.  No allocation happens after a device's workspace
+// exists, so every launch can be captured in a CUDA graph.
+#include "../../include/pkv.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "pkv_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kDefaultWorkspace = size_t(1) << 30;
+constexpr int64_t kNumCounters = int64_t(1) << 20;
+
+struct DeviceState {
+  pkv::Workspace ws;
+  cudaEvent_t order_event = nullptr;
+  cudaStream_t last_stream = nullptr;
+  bool has_last = false;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// ------------------------------------------------------------ workspace --
+int init_locked(int device, size_t partial_bytes) {
+  DeviceState& st = g_dev[device];
+  if (st.ws.base) return PKV_OK;
+  if (partial_bytes == 0) partial_bytes = kDefaultWorkspace;
+  partial_bytes = (partial_bytes + 255) / 256 * 256;
+  const size_t head = 512 + size_t(kNumCounters) * 4;  // err + sched, counters
+  const size_t total = head + partial_bytes;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaError_t e = cudaSetDevice(device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  void* base = nullptr;
+  e = cudaMalloc(&base, total);
+  if (e != cudaSuccess) {
+    cudaSetDevice(prev);
+    return cuda_fail(e, "workspace cudaMalloc");
+  }
+  e = cudaMemset(base, 0, head);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&st.order_event, cudaEventDisableTiming);
+  int sms = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(base);
+    cudaSetDevice(prev);
+    return cuda_fail(e, "workspace init");
+  }
+  uint8_t* b = static_cast<uint8_t*>(base);
+  st.ws.base = base;
+  st.ws.bytes = total;
+  st.ws.err = reinterpret_cast<int*>(b);
+  st.ws.sched = reinterpret_cast<int*>(b + 256);
+  st.ws.counters = reinterpret_cast<int*>(b + 512);
+  st.ws.num_counters = kNumCounters;
+  st.ws.partials = reinterpret_cast<float*>(b + head);
+  st.ws.partial_bytes = partial_bytes;
+  st.ws.num_sms = sms;
+  cudaSetDevice(prev);
+  return PKV_OK;
+}
+
+// Workspace of the current device, allocating it on first use (refused while
+// the stream is being captured: allocation would not be part of the graph).
+int workspace_for(cudaStream_t stream, int* device, DeviceState** out, bool* capturing) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device %d", dev);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  *capturing = cs != cudaStreamCaptureStatusNone;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_dev[dev].ws.base) {
+    if (*capturing)
+      return fail(PKV_ERR_CAPTURE,
+                  "the workspace of device %d must be allocated (pkv_init or one eager call) "
+                  "before CUDA graph capture", dev);
+    const int rc = init_locked(dev, 0);
+    if (rc != PKV_OK) return rc;
+  }
+  *device = dev;
+  *out = &g_dev[dev];
+  return PKV_OK;
+}
+
+// Launches sharing a workspace must be ordered: a call on a new stream first
+// waits for the stream of the previous call (outside graph capture).
+int order_streams(DeviceState* st, cudaStream_t stream, bool capturing) {
+  if (capturing) return PKV_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (st->has_last && st->last_stream != stream) {
+    cudaError_t e = cudaEventRecord(st->order_event, st->last_stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, st->order_event, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cross-stream ordering");
+  }
+  st->last_stream = stream;
+  st->has_last = true;
+  return PKV_OK;
+}
+
+// ------------------------------------------------------------ validation --
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_tensor(const pkv_tensor* t, const char* name, int dtype, int ndim) {
+  if (!t) return fail(PKV_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!t->data) return fail(PKV_ERR_INVALID_ARG, "%s has a NULL data pointer", name);
+  if (t->dtype != dtype)
+    return fail(PKV_ERR_INVALID_ARG, "%s has dtype %d, expected %d", name, t->dtype, dtype);
+  if (t->ndim != ndim)
+    return fail(PKV_ERR_INVALID_ARG, "%s has %d dims, expected %d", name, t->ndim, ndim);
+  for (int i = 0; i < ndim; ++i)
+    if (t->shape[i] < 0 || t->stride[i] < 0)
+      return fail(PKV_ERR_INVALID_ARG, "%s has a negative size or stride", name);
+  return PKV_OK;
+}
+
+// ---------------------------------------------------------- tensor maps --
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int get_encoder(EncodeTiledFn* fn) {
+  static EncodeTiledFn cached = nullptr;
+  static std::once_flag once;
+  static cudaError_t status = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    status = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                              cudaEnableDefault, &q);
+    if (status == cudaSuccess && q == cudaDriverEntryPointSuccess) cached = (EncodeTiledFn)p;
+  });
+  if (!cached) {
+    if (status != cudaSuccess) return cuda_fail(status, "cuTensorMapEncodeTiled lookup");
+    return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  }
+  *fn = cached;
+  return PKV_OK;
+}
+
+}  // namespace
+
+// =================================================================== ABI ==
+extern "C" {
+
+PKV_API int pkv_version(void) { return 100; }
+
+PKV_API const char* pkv_last_error(void) { return g_last_error.c_str(); }
+
+PKV_API int pkv_init(int device, size_t workspace_bytes) {
+  if (device < 0 || device >= kMaxDevices) return fail(PKV_ERR_INVALID_ARG, "device %d", device);
+  int count = 0;
+  cudaError_t e = cudaGetDeviceCount(&count);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+  if (device >= count) return fail(PKV_ERR_INVALID_ARG, "device %d of %d", device, count);
+  // refuse while the legacy stream of the device is capturing
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(device);
+  e = cudaStreamIsCapturing(cudaStreamPerThread, &cs);
+  cudaSetDevice(prev);
+  if (e == cudaSuccess && cs != cudaStreamCaptureStatusNone)
+    return fail(PKV_ERR_CAPTURE, "pkv_init during stream capture");
+  std::lock_guard<std::mutex> lk(g_mu);
+  return init_locked(device, workspace_bytes);
+}
+
+PKV_API int pkv_shutdown(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int prev = 0;
+  cudaGetDevice(&prev);
+  for (int d = 0; d < kMaxDevices; ++d) {
+    DeviceState& st = g_dev[d];
+    if (!st.ws.base) continue;
+    cudaSetDevice(d);
+    cudaDeviceSynchronize();
+    cudaFree(st.ws.base);
+    if (st.order_event) cudaEventDestroy(st.order_event);
+    st = DeviceState();
+  }
+  cudaSetDevice(prev);
+  return PKV_OK;
+}
+
+PKV_API int pkv_check_errors(int device, int32_t* flags) {
+  if (!flags) return fail(PKV_ERR_INVALID_ARG, "flags is NULL");
+  *flags = 0;
+  if (device < 0 || device >= kMaxDevices) return fail(PKV_ERR_INVALID_ARG, "device %d", device);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[device];
+  if (!st.ws.base) return PKV_OK;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(device);
+  int32_t v = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&v, st.ws.err, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(st.ws.err, 0, 4);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  cudaSetDevice(prev);
+  if (e != cudaSuccess) return cuda_fail(e, "pkv_check_errors");
+  *flags = v;
+  if (v == 0) return PKV_OK;
+  if (v & (pkv::DEVERR_BAD_BLOCK | pkv::DEVERR_SEQ_TOO_LONG))
+    return fail(PKV_ERR_BAD_BLOCK_TABLE, "device error word 0x%x: bad block table or seq_lens", v);
+  return fail(PKV_ERR_CUDA, "device error word 0x%x", v);
+}
+
+PKV_API int pkv_check_counters(int device, int64_t* nonzero) {
+  if (!nonzero) return fail(PKV_ERR_INVALID_ARG, "nonzero is NULL");
+  *nonzero = 0;
+  if (device < 0 || device >= kMaxDevices) return fail(PKV_ERR_INVALID_ARG, "device %d", device);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[device];
+  if (!st.ws.base) return PKV_OK;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(device);
+  const size_t n = 64 + size_t(st.ws.num_counters);
+  int32_t* host = static_cast<int32_t*>(malloc(n * 4));
+  if (!host) {
+    cudaSetDevice(prev);
+    return fail(PKV_ERR_INVALID_ARG, "host allocation failed");
+  }
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(host, st.ws.sched, 64 * 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(host + 64, st.ws.counters, size_t(st.ws.num_counters) * 4,
+                   cudaMemcpyDeviceToHost);
+  cudaSetDevice(prev);
+  if (e != cudaSuccess) {
+    free(host);
+    return cuda_fail(e, "pkv_check_counters");
+  }
+  int64_t c = 0;
+  for (size_t i = 0; i < n; ++i) c += host[i] != 0;
+  free(host);
+  *nonzero = c;
+  return PKV_OK;
+}
+
+PKV_API int pkv_num_kv_splits(int max_seq_len, int batch, int qlen, int num_heads, int sm_count,
+                              int block_h, double occupancy, int min_work_per_split,
+                              int max_splits) {
+  if (sm_count <= 0 || block_h <= 0 || qlen <= 0 || num_heads <= 0 || !(occupancy >= 0.0))
+    return fail(PKV_ERR_INVALID_ARG, "pkv_num_kv_splits: bad argument");
+  auto cdiv = [](long long a, long long b) { return (a + b - 1) / b; };
+  const long long row_blocks = cdiv((long long)qlen * num_heads, block_h);
+  const long long per_split = (long long)(batch > 1 ? batch : 1) * row_blocks;
+  const long long ideal =
+      cdiv(max_seq_len > 1 ? max_seq_len : 1, min_work_per_split > 1 ? min_work_per_split : 1);
+  long long slots = (long long)(occupancy * sm_count);
+  if (slots < 1) slots = 1;
+  long long n;
+  if (per_split <= slots) {
+    n = slots / per_split;  // one dispatch round holds this many splits of every request
+  } else {
+    long long hi = ideal < max_splits ? ideal : max_splits;
+    if (hi < 1) hi = 1;
+    // cost(n) = rounds(n) / n: the idle tail of the last dispatch round
+    double best = 1e300;
+    for (long long k = 1; k <= hi; ++k) {
+      const double c = double(cdiv(k * per_split, slots)) / double(k);
+      if (c < best) best = c;
+    }
+    n = 1;
+    for (long long k = 1; k <= hi; ++k) {
+      const double c = double(cdiv(k * per_split, slots)) / double(k);
+      if (c <= best * 1.05) {
+        n = k;
+        break;
+      }
+    }
+  }
+  long long r = n;
+  if (ideal < r) r = ideal;
+  if (2LL * sm_count < r) r = 2LL * sm_count;
+  if (r < 1) r = 1;
+  return (int)r;
+}
+
+PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cache,
+                                  const pkv_tensor* block_table, const pkv_tensor* seq_lens,
+                                  const pkv_tensor* sinks, int window, float scale,
+                                  int page_size, int num_kv_splits, const pkv_tensor* out,
+                                  const pkv_tensor* lse, void* stream_ptr) {
+  int rc;
+  if ((rc = check_tensor(q, "q", PKV_DTYPE_BF16, 3))) return rc;
+  if ((rc = check_tensor(kv_cache, "kv_cache", PKV_DTYPE_BF16, 4))) return rc;
+  if ((rc = check_tensor(block_table, "block_table", PKV_DTYPE_I32, 2))) return rc;
+  if ((rc = check_tensor(seq_lens, "seq_lens", PKV_DTYPE_I32, 1))) return rc;
+  if ((rc = check_tensor(out, "out", PKV_DTYPE_BF16, 3))) return rc;
+  if (sinks && (rc = check_tensor(sinks, "sinks", PKV_DTYPE_F32, 1))) return rc;
+  if (lse && (rc = check_tensor(lse, "lse", PKV_DTYPE_F32, 2))) return rc;
+
+  const int64_t B = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  const int64_t nb = kv_cache->shape[0], Hkv = kv_cache->shape[1];
+  if (D != pkv::kGqaHeadDim)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %lld (only 128 is built)", (long long)D);
+  if (kv_cache->shape[3] != 2 * D)
+    return fail(PKV_ERR_INVALID_ARG, "kv_cache last dim %lld, expected [K | V] = 256",
+                (long long)kv_cache->shape[3]);
+  if (Hkv <= 0 || Hq != pkv::kGqaGroup * Hkv)
+    return fail(PKV_ERR_UNSUPPORTED, "num_q_heads %lld must be 8 x num_kv_heads %lld",
+                (long long)Hq, (long long)Hkv);
+  if (page_size != 16 && page_size != 32)
+    return fail(PKV_ERR_UNSUPPORTED, "page_size %d (16 and 32 are built)", page_size);
+  if (kv_cache->shape[2] != page_size)
+    return fail(PKV_ERR_INVALID_ARG, "kv_cache.shape[2] %lld != page_size %d",
+                (long long)kv_cache->shape[2], page_size);
+  if (nb < 1 || nb >= (int64_t(1) << 31))
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks %lld", (long long)nb);
+  if (block_table->shape[0] != B || seq_lens->shape[0] != B)
+    return fail(PKV_ERR_INVALID_ARG, "block_table / seq_lens batch mismatch");
+  if (out->shape[0] != B || out->shape[1] != Hq || out->shape[2] != D)
+    return fail(PKV_ERR_INVALID_ARG, "out shape mismatch");
+  if (sinks && sinks->shape[0] != Hq) return fail(PKV_ERR_INVALID_ARG, "sinks must be [Hq]");
+  if (sinks && sinks->shape[0] > 1 && sinks->stride[0] != 1)
+    return fail(PKV_ERR_INVALID_ARG, "sinks must be contiguous");
+  if (lse && (lse->shape[0] != B || lse->shape[1] != Hq))
+    return fail(PKV_ERR_INVALID_ARG, "lse must be [B, Hq]");
+  if (block_table->shape[1] < 1 || block_table->shape[1] > (int64_t(1) << 30))
+    return fail(PKV_ERR_INVALID_ARG, "block_table width %lld", (long long)block_table->shape[1]);
+  if (block_table->stride[1] != 1 && block_table->shape[1] > 1)
+    return fail(PKV_ERR_INVALID_ARG, "block_table rows must be contiguous");
+  if (seq_lens->stride[0] != 1 && B > 1)
+    return fail(PKV_ERR_INVALID_ARG, "seq_lens must be contiguous");
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (num_kv_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_splits < 0");
+  if (B > pkv::kGqaMaxBatch)
+    return fail(PKV_ERR_UNSUPPORTED, "batch %lld > %d", (long long)B, pkv::kGqaMaxBatch);
+  // layout rules of the HND page cache and 16-byte vector access
+  if (q->stride[2] != 1 || out->stride[2] != 1 || kv_cache->stride[3] != 1 ||
+      kv_cache->stride[2] != 2 * D)
+    return fail(PKV_ERR_INVALID_ARG, "q/out last dim and kv_cache rows must be contiguous");
+  if (q->stride[0] % 8 || q->stride[1] % 8 || out->stride[0] % 8 || out->stride[1] % 8 ||
+      kv_cache->stride[0] % 8 || kv_cache->stride[1] % 8)
+    return fail(PKV_ERR_ALIGNMENT, "strides of q, out and kv_cache must be multiples of 8");
+  if (!aligned16(q->data) || !aligned16(out->data) || !aligned16(kv_cache->data))
+    return fail(PKV_ERR_ALIGNMENT, "q, out and kv_cache must be 16-byte aligned");
+  if (B == 0) return PKV_OK;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int dev = 0;
+  DeviceState* st = nullptr;
+  bool capturing = false;
+  if ((rc = workspace_for(stream, &dev, &st, &capturing))) return rc;
+  const pkv::Workspace& ws = st->ws;
+
+  const int64_t item_bytes = int64_t(pkv::kGqaPartialFloats + pkv::kGqaMlFloats) * 4;
+  const int64_t max_items = int64_t(ws.partial_bytes) / item_bytes;
+  const int64_t bh = B * Hkv;
+  if (bh > ws.num_counters)
+    return fail(PKV_ERR_WORKSPACE, "%lld (request, kv head) pairs exceed %lld counters",
+                (long long)bh, (long long)ws.num_counters);
+  int64_t cap = num_kv_splits;
+  if (cap == 0) {
+    cap = max_items / bh;
+    if (cap > 256) cap = 256;
+    if (cap < 1) cap = 1;
+  }
+  if (bh * cap > max_items)
+    return fail(PKV_ERR_WORKSPACE, "workspace holds %lld split partials, %lld x %lld needed",
+                (long long)max_items, (long long)bh, (long long)cap);
+
+  EncodeTiledFn encode = nullptr;
+  if ((rc = get_encoder(&encode))) return rc;
+  alignas(64) CUtensorMap map;
+  const cuuint64_t gdim[4] = {cuuint64_t(2 * D), cuuint64_t(page_size), cuuint64_t(Hkv),
+                              cuuint64_t(nb)};
+  const cuuint64_t gstride[3] = {cuuint64_t(kv_cache->stride[2]) * 2,
+                                 cuuint64_t(kv_cache->stride[1]) * 2,
+                                 cuuint64_t(kv_cache->stride[0]) * 2};
+  const cuuint32_t box[4] = {64, cuuint32_t(page_size), 1, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, kv_cache->data, gdim, gstride,
+                       box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS)
+    return fail(PKV_ERR_INVALID_ARG, "cuTensorMapEncodeTiled rejected the kv_cache layout (%d)",
+                (int)cr);
+
+  pkv::GqaParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = static_cast<const uint16_t*>(q->data);
+  p.q_sb = q->stride[0];
+  p.q_sh = q->stride[1];
+  p.bt = static_cast<const int32_t*>(block_table->data);
+  p.bt_sb = block_table->stride[0];
+  p.max_blocks = int(block_table->shape[1]);
+  p.num_blocks = int(nb);
+  p.seq_lens = static_cast<const int32_t*>(seq_lens->data);
+  p.sinks = sinks ? static_cast<const float*>(sinks->data) : nullptr;
+  p.out = static_cast<uint16_t*>(out->data);
+  p.o_sb = out->stride[0];
+  p.o_sh = out->stride[1];
+  p.lse = lse ? static_cast<float*>(lse->data) : nullptr;
+  p.lse_sb = lse ? lse->stride[0] : 0;
+  p.lse_sh = lse ? lse->stride[1] : 0;
+  p.B = int(B);
+  p.Hkv = int(Hkv);
+  p.window = window;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale = scale;
+  p.cap = int(cap);
+  p.min_pages = page_size == 16 ? 4 : 2;
+  const int64_t grid64 = std::min<int64_t>(ws.num_sms, bh * cap);
+  const int grid = int(grid64 < 1 ? 1 : grid64);
+  p.target_items = grid * 24;
+  p.part_o = ws.partials;
+  p.part_ml = ws.partials + max_items * pkv::kGqaPartialFloats;
+  p.max_items = max_items;
+  p.counters = ws.counters;
+  p.sched = ws.sched;
+  p.err = ws.err;
+
+  if ((rc = order_streams(st, stream, capturing))) return rc;
+  const cudaError_t e = pkv::launch_gqa_decode(p, map, page_size, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gqa decode launch");
+  return PKV_OK;
+}
+
+PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_cache,
+                                const pkv_tensor* block_table, const pkv_tensor* seq_lens,
+                                const pkv_tensor* real_seq_lens, int qlen, float scale,
+                                int page_size, const pkv_tensor* k_scale, const pkv_tensor* out,
+                                const pkv_tensor* lse, int num_kv_splits, void* stream) {
+  (void)q; (void)latent_cache; (void)block_table; (void)seq_lens; (void)real_seq_lens;
+  (void)qlen; (void)scale; (void)page_size; (void)k_scale; (void)out; (void)lse;
+  (void)num_kv_splits; (void)stream;
+  return fail(PKV_ERR_UNSUPPORTED, "the MLA verify kernel is not built yet");
+}
+
+}  // extern "C"

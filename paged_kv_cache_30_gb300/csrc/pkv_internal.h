@@ -1,0 +1,72 @@
+// pkv_internal.h -- declarations shared by the host launcher (api.cpp) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// Device-side error bits, OR-ed into the workspace error word and read back by
+// pkv_check_errors().
+enum : int {
+  DEVERR_BAD_BLOCK = 1,      // a block-table entry outside [0, num_blocks)
+  DEVERR_SEQ_TOO_LONG = 2,   // seq_len needs more pages than the block table holds
+  DEVERR_WAIT_TIMEOUT = 4,   // a pipeline wait gave up (the kernel drained and returned)
+  DEVERR_ITEM_OVERFLOW = 8,  // more work items than the workspace holds
+};
+
+// Per-device workspace carved out of one allocation (see api.cpp).
+struct Workspace {
+  void* base = nullptr;
+  size_t bytes = 0;
+  float* partials = nullptr;  // split partials, reused by both paths
+  size_t partial_bytes = 0;
+  int* counters = nullptr;    // self-resetting arrival counters
+  int64_t num_counters = 0;
+  int* sched = nullptr;       // [0] work-queue head, [1] exited CTAs (both self-resetting)
+  int* err = nullptr;         // device error word
+  int num_sms = 0;
+};
+
+// ---------------------------------------------------------------- GQA --
+constexpr int kGqaHeadDim = 128;
+constexpr int kGqaGroup = 8;         // query heads per kv head
+constexpr int kGqaMaxBatch = 2048;   // requests per call (device-side scheduler table)
+constexpr int kGqaPartialFloats = kGqaGroup * kGqaHeadDim;  // O partial of one work item
+constexpr int kGqaMlFloats = 2 * kGqaGroup;                 // m[8], l[8] of one work item
+
+struct GqaParams {
+  const uint16_t* q;  // bf16 [B, Hq, 128]
+  int64_t q_sb, q_sh;
+  const int32_t* bt;
+  int64_t bt_sb;
+  int max_blocks;
+  int num_blocks;
+  const int32_t* seq_lens;
+  const float* sinks;  // [Hq] or null
+  uint16_t* out;       // bf16 [B, Hq, 128]
+  int64_t o_sb, o_sh;
+  float* lse;          // [B, Hq] or null
+  int64_t lse_sb, lse_sh;
+  int B, Hkv;
+  int window;          // <= 0: all keys
+  float scale_log2;    // scale * log2(e)
+  float scale;
+  int cap;             // max splits per (request, kv head)
+  int min_pages;       // fewest pages a split may hold
+  int target_items;    // desired number of work items per launch
+  float* part_o;       // [max_items][8][128]
+  float* part_ml;      // [max_items][16]
+  int64_t max_items;
+  int* counters;       // [B * Hkv]
+  int* sched;
+  int* err;
+};
+
+// Launch the GQA decode kernel for page size 16 or 32 on `grid` CTAs.
+cudaError_t launch_gqa_decode(const GqaParams& p, const CUtensorMap& kv_map, int page_size,
+                              int grid, cudaStream_t stream);
+size_t gqa_smem_bytes(int page_size);
+
+}  // namespace pkv

@@ -1,0 +1,146 @@
+"""CPU-side checks of the C ABI: the library loads, exports every entry point
+declared in include/pkv.h, rejects bad arguments before touching a GPU, and
+its host-only split-cap heuristic follows the verify page's contract."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_30_gb300 as pkv
+from paged_kv_cache_30_gb300 import build as pkv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkv_build.build()
+    return pkv.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for n in ("pkv_paged_decode_attn", "pkv_mla_verify_attn", "pkv_init", "pkv_num_kv_splits",
+              "pkv_check_errors", "pkv_check_counters", "pkv_last_error", "pkv_shutdown",
+              "pkv_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"{name} is declared in pkv.h but not exported"
+
+
+def test_version(lib):
+    assert pkv.version() >= 100
+
+
+def _t(shape, dtype, strides=None, ptr=0x10000):
+    d = pkv.PkvTensor()
+    d.data = ptr
+    d.dtype = dtype
+    d.ndim = len(shape)
+    if strides is None:
+        strides, acc = [], 1
+        for s in reversed(shape):
+            strides.insert(0, acc)
+            acc *= s
+    for i, (s, st) in enumerate(zip(shape, strides)):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def _gqa_args(B=2, Hq=16, Hkv=2, D=128, P=16, nb=64, maxb=8):
+    return dict(
+        q=_t([B, Hq, D], pkv.DTYPE_BF16), kv=_t([nb, Hkv, P, 2 * D], pkv.DTYPE_BF16),
+        bt=_t([B, maxb], pkv.DTYPE_I32), sl=_t([B], pkv.DTYPE_I32),
+        out=_t([B, Hq, D], pkv.DTYPE_BF16, ptr=0x20000), lse=_t([B, Hq], pkv.DTYPE_F32))
+
+
+def _call(lib, a, sinks=None, window=0, scale=0.088, P=16, cap=0):
+    r = ctypes.byref
+    return lib.pkv_paged_decode_attn(r(a["q"]), r(a["kv"]), r(a["bt"]), r(a["sl"]),
+                                     r(sinks) if sinks is not None else None, window, scale, P,
+                                     cap, r(a["out"]), r(a["lse"]), None)
+
+
+@pytest.mark.parametrize("mutate,code", [
+    (lambda a: a.update(q=_t([2, 16, 64], pkv.DTYPE_BF16)), -2),               # head dim 64
+    (lambda a: a.update(q=_t([2, 12, 128], pkv.DTYPE_BF16)), -2),              # Hq != 8 Hkv
+    (lambda a: a.update(kv=_t([64, 2, 8, 256], pkv.DTYPE_BF16)), -1),          # P mismatch
+    (lambda a: a.update(q=_t([2, 16, 128], pkv.DTYPE_F32)), -1),               # dtype
+    (lambda a: a.update(bt=_t([3, 8], pkv.DTYPE_I32)), -1),                    # batch mismatch
+    (lambda a: a.update(q=_t([2, 16, 128], pkv.DTYPE_BF16, ptr=0x10008)), -3),  # alignment
+    (lambda a: a.update(kv=_t([64, 2, 16, 256], pkv.DTYPE_BF16, [8196, 4098, 256, 1])), -3),
+    (lambda a: a.update(kv=_t([64, 2, 16, 256], pkv.DTYPE_BF16, [8192, 4096, 512, 1])), -1),
+    (lambda a: a.update(q=_t([4096, 16, 128], pkv.DTYPE_BF16),
+                        bt=_t([4096, 8], pkv.DTYPE_I32), sl=_t([4096], pkv.DTYPE_I32),
+                        out=_t([4096, 16, 128], pkv.DTYPE_BF16),
+                        lse=_t([4096, 16], pkv.DTYPE_F32)), -2),               # batch > 2048
+])
+def test_gqa_validation_rejects_before_any_cuda_call(lib, mutate, code):
+    a = _gqa_args()
+    mutate(a)
+    assert _call(lib, a) == code
+    assert pkv.last_error()
+
+
+def test_gqa_validation_page_size_and_args(lib):
+    a = _gqa_args()
+    assert _call(lib, a, P=8) == -2
+    assert _call(lib, a, cap=-1) == -1
+    assert _call(lib, a, scale=float("inf")) == -1
+    bad_sinks = _t([8], pkv.DTYPE_F32)
+    assert _call(lib, a, sinks=bad_sinks) == -1
+    r = ctypes.byref
+    assert lib.pkv_paged_decode_attn(None, r(a["kv"]), r(a["bt"]), r(a["sl"]), None, 0, 1.0,
+                                     16, 0, r(a["out"]), None, None) == -1
+
+
+def test_gqa_empty_batch_is_a_no_op(lib):
+    a = _gqa_args(B=0)
+    assert _call(lib, a) == 0
+
+
+# ---------------------------------------------------- split-cap heuristic --
+# Contract ("vllm.v1.attention.ops.triton_decode_attention", verify_num_kv_splits):
+# programs per split = batch x row blocks; if they fit one round of
+# occupancy x SMs slots, use slots // programs; otherwise the n <= max_splits
+# minimising rounds(n)/n, the fewest within 5 % of the best; clamp to
+# [1, min(ideal, 2 x SMs)] with ideal = cdiv(max_seq_len, min_work_per_split).
+
+def test_num_kv_splits_single_round(lib):
+    # 2 requests x cdiv(4*128, 64) = 8 row blocks -> 16 programs; 152 slots -> 9
+    assert pkv.num_kv_splits(8192, 2, 4, 128, 152, 64, 1.0, 64, 8) == 9
+    # capped by ideal = cdiv(100, 64) = 2
+    assert pkv.num_kv_splits(100, 2, 4, 128, 152, 64, 1.0, 64, 8) == 2
+
+
+def test_num_kv_splits_multi_round():
+    # 32 requests x 8 row blocks = 256 programs on 152 slots:
+    # n=1: 2 rounds -> 2.0; n=2: cdiv(512,152)=4 -> 2.0; n=3: 6/3=2.0;
+    # n=4: cdiv(1024,152)=7 -> 1.75; n=5: 9/5=1.8; n=6: 11/6=1.83;
+    # n=7: 12/7=1.714; n=8: 14/8=1.75  -> best 1.714; within 5%: <= 1.8 -> n=4
+    assert pkv.num_kv_splits(8192, 32, 4, 128, 152, 64, 1.0, 64, 8) == 4
+    # max_splits 1 -> 1
+    assert pkv.num_kv_splits(8192, 32, 4, 128, 152, 64, 1.0, 64, 1) == 1
+
+
+def test_num_kv_splits_clamps():
+    # 2 x SMs cap: one program per split, 1000 slots, ideal large -> min(1000, 2*4)
+    assert pkv.num_kv_splits(1 << 20, 1, 1, 1, 4, 64, 250.0, 1, 8) == 8
+    assert pkv.num_kv_splits(0, 0, 1, 8, 152, 64, 1.0, 64, 8) == 1
+    with pytest.raises(pkv.PkvError):
+        pkv.num_kv_splits(8192, 2, 4, 128, 0, 64, 1.0, 64, 8)
+
+
+def test_mla_entry_point_is_exported(lib):
+    assert hasattr(lib, "pkv_mla_verify_attn")

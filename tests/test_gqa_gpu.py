@@ -1,0 +1,328 @@
+"""GPU parity of the GQA paged decode kernel against the fp64 oracle, through
+the C ABI (pkv_paged_decode_attn via the ctypes binding)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_30_gb300 as pkv
+from paged_kv_cache_30_gb300 import workloads as W
+from tests.gpu_helpers import TOL_LSE, TOL_OUT, compare, dev, run_gqa
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    pkv.load_library()
+    pkv.init(0)
+
+
+def oracle_gqa(prob, rows=None):
+    return oracle.gqa_decode(prob.q, prob.kv_cache, prob.block_table, prob.seq_lens,
+                             prob.sinks, prob.window, prob.scale, prob.page_size, rows=rows)
+
+
+def check(prob, cap=None, what=""):
+    out, lse = run_gqa(prob, cap)
+    ref_out, ref_lse = oracle_gqa(prob)
+    B, Hq, D = prob.q.shape
+    return compare(out, lse, ref_out.reshape(B, Hq, D), ref_lse.reshape(B, Hq), what=what)
+
+
+# ------------------------------------------------ the pages' worked example --
+
+def test_block_table_worked_example_gpu():
+    g = json.load(open(os.path.join(HERE, "golden", "block_table_example.json")))
+    P, Hq, Hkv, D = g["page_size"], 8, 1, 128
+    bt = np.array(g["block_table"], dtype=np.int32)
+    L = np.array(g["seq_lens"], dtype=np.int32)
+    kv = torch.full((g["num_pages"], Hkv, P, 2 * D), float("nan"))
+    for b in range(len(L)):
+        for j in range(L[b]):
+            page, slot = int(bt[b, j // P]), j % P
+            kv[page, :, slot, :D] = 0.0
+            kv[page, :, slot, D:] = (32 * page + slot) / 256.0
+    prob = W.GQAProblem(q=W.normal((3, Hq, D), 5), kv_cache=kv.to(torch.bfloat16),
+                        block_table=torch.from_numpy(bt), seq_lens=torch.from_numpy(L),
+                        sinks=None, window=0, scale=1 / math.sqrt(D), page_size=P)
+    for cap in (1, 2, 0):
+        out, lse = run_gqa(prob, cap)
+        for b, e in enumerate(g["expected"]):
+            n, d = map(int, e["out"].split("/"))
+            exact = n / d
+            # the GPU sums exact bf16 values in fp32 and rounds once to bf16
+            assert np.all(np.abs(out[b] - exact) <= exact * 2.0 ** -8), (cap, b)
+            assert np.max(np.abs(lse[b] - math.log(float(e["lse"][3:-1])))) <= 1e-5
+
+
+# ----------------------------------------------------------- tiny workload --
+
+@pytest.mark.parametrize("seed", range(5))
+def test_tiny_gqa_config(seed):
+    check(W.tiny_gqa(seed), what=f"tiny seed {seed}")
+
+
+@pytest.mark.parametrize("seed,B,Hkv,P,Lmin,Lmax,sinks,window,cap", [
+    (0, 3, 1, 16, 1, 700, True, 0, 0),
+    (1, 5, 2, 16, 1, 1500, False, 0, 3),
+    (2, 4, 3, 32, 1, 2100, True, 0, 0),
+    (3, 6, 1, 32, 1, 999, True, 128, 0),
+    (4, 7, 2, 16, 100, 3000, True, 37, 5),
+    (5, 3, 4, 16, 16, 16, True, 0, 1),
+    (6, 9, 1, 16, 1, 40, True, 0, 64),
+    (7, 2, 2, 32, 1000, 5000, True, 1, 0),
+    (8, 8, 1, 32, 31, 33, False, 32, 2),
+])
+def test_random_cases(seed, B, Hkv, P, Lmin, Lmax, sinks, window, cap):
+    prob = W.gqa_problem(seed, B, 8 * Hkv, Hkv, P, "uniform", Lmin, Lmax, sinks=sinks,
+                         window=window, num_kv_splits=cap)
+    check(prob, what=f"case {seed}")
+
+
+def test_edge_lengths():
+    """Empty rows, one key, exact page multiples, one past a page, window 1."""
+    L = np.array([0, 1, 16, 17, 32, 33, 15, 0, 2, 48], dtype=np.int32)
+    for window in (0, 1, 16, 17, 100):
+        for P in (16, 32):
+            prob = W.gqa_problem(11, len(L), 16, 2, P, "const", 1, 64, seq_lens=L, sinks=True,
+                                 window=window)
+            for cap in (1, 3, 0):
+                check(prob, cap, what=f"edge P={P} W={window} cap={cap}")
+
+
+def test_nan_poisoned_unattended_slots_stay_finite():
+    for P, window in ((16, 0), (32, 0), (16, 23), (32, 50)):
+        prob = W.gqa_problem(12, 6, 16, 2, P, "uniform", 1, 600, sinks=True, window=window,
+                             poison_unused=True)
+        check(prob, what=f"poison P={P} W={window}")
+
+
+def test_no_sinks_no_lse():
+    prob = W.gqa_problem(13, 4, 8, 1, 16, "uniform", 1, 500)
+    out, lse = run_gqa(prob, lse=False)
+    ref_out, _ = oracle_gqa(prob)
+    assert lse is None
+    assert np.max(np.abs(out.reshape(ref_out.shape) - ref_out)) <= TOL_OUT
+
+
+def test_strided_views():
+    """q/out with padded batch rows and a cache whose kv heads are padded."""
+    prob = W.gqa_problem(14, 4, 16, 2, 16, "uniform", 1, 400, sinks=True)
+    B, Hq, D = prob.q.shape
+    qbig = torch.zeros((B, Hq + 3, D), dtype=torch.bfloat16, device="cuda")
+    qbig[:, :Hq] = prob.q.cuda()
+    q = qbig[:, :Hq]
+    nb, Hkv, P, D2 = prob.kv_cache.shape
+    kvbig = torch.zeros((nb, Hkv + 1, P, D2), dtype=torch.bfloat16, device="cuda")
+    kvbig[:, :Hkv] = prob.kv_cache.cuda()
+    kv = kvbig[:, :Hkv]
+    outbig = torch.zeros((B, Hq + 8, D), dtype=torch.bfloat16, device="cuda")
+    out = outbig[:, 8:]
+    lse = torch.empty((Hq, B), device="cuda").t()
+    pkv.paged_decode_attn(q, kv, prob.block_table.cuda(), prob.seq_lens.cuda(),
+                          prob.sinks.cuda(), 0, prob.scale, 16, 0, out, lse)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle_gqa(prob)
+    compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out.reshape(B, Hq, D),
+            ref_lse.reshape(B, Hq), what="strided")
+    assert torch.all(outbig[:, :8] == 0)
+
+
+# ------------------------------------------------------------- invariants --
+
+def test_split_count_invariance_and_counters_reset():
+    prob = W.gqa_problem(15, 4, 32, 4, 32, "uniform", 2000, 9000, sinks=True)
+    ref_out, ref_lse = oracle_gqa(prob)
+    outs = []
+    for cap in (1, 2, 8, 32, 132, 0):
+        out, lse = run_gqa(prob, cap)
+        compare(out, lse, ref_out.reshape(out.shape), ref_lse.reshape(lse.shape),
+                what=f"cap {cap}")
+        outs.append((out, lse))
+    for out, lse in outs[1:]:
+        assert np.max(np.abs(out - outs[0][0])) <= 2e-3
+        assert np.max(np.abs(lse - outs[0][1])) <= 1e-4
+    assert pkv.check_counters(0) == 0
+
+
+def test_physical_page_permutation_is_bitwise_invariant():
+    prob = W.gqa_problem(16, 5, 16, 2, 16, "uniform", 1, 3000, sinks=True)
+    out1, lse1 = run_gqa(prob)
+    nb = prob.kv_cache.shape[0]
+    perm = torch.from_numpy(np.random.default_rng(5).permutation(nb))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(nb)
+    bt2 = prob.block_table.clone()
+    m = bt2 >= 0
+    bt2[m] = inv[bt2[m].long()].int()
+    prob2 = W.GQAProblem(q=prob.q, kv_cache=prob.kv_cache[perm].contiguous(), block_table=bt2,
+                         seq_lens=prob.seq_lens, sinks=prob.sinks, window=0, scale=prob.scale,
+                         page_size=16)
+    out2, lse2 = run_gqa(prob2)
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
+
+
+def test_many_calls_leave_counters_at_zero():
+    prob = W.gqa_problem(17, 8, 16, 2, 16, "uniform", 1, 4000, sinks=True)
+    d = dict(q=dev(prob.q), kv=dev(prob.kv_cache), bt=dev(prob.block_table),
+             sl=dev(prob.seq_lens), sinks=dev(prob.sinks))
+    out = torch.empty_like(d["q"])
+    for i in range(300):
+        pkv.paged_decode_attn(d["q"], d["kv"], d["bt"], d["sl"], d["sinks"], 0, prob.scale, 16,
+                              (0, 1, 4, 16)[i % 4], out, None)
+    torch.cuda.synchronize()
+    assert pkv.check_counters(0) == 0
+    ref_out, _ = oracle_gqa(prob)
+    assert np.max(np.abs(out.float().cpu().numpy().reshape(ref_out.shape) - ref_out)) <= TOL_OUT
+
+
+def test_cuda_graph_replay_with_new_lengths_and_tables():
+    """The launch shape depends only on the batch: a captured call replays
+    correctly after seq_lens and block_table change on the device."""
+    pa = W.gqa_problem(18, 6, 16, 2, 16, "uniform", 1, 2000, sinks=True, max_blocks=200,
+                       pool_pages=1200)
+    pb = W.gqa_problem(19, 6, 16, 2, 16, "uniform", 1, 3000, sinks=True, max_blocks=200,
+                       pool_pages=1200)
+    pb.q = pa.q
+    pb.sinks = pa.sinks
+    pb.kv_cache = pa.kv_cache
+    q, kv, sinks = dev(pa.q), dev(pa.kv_cache), dev(pa.sinks)
+    bt, sl = dev(pa.block_table), dev(pa.seq_lens)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], device="cuda")
+    s = torch.cuda.Stream()
+    pkv.paged_decode_attn(q, kv, bt, sl, sinks, 0, pa.scale, 16, 0, out, lse, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.paged_decode_attn(q, kv, bt, sl, sinks, 0, pa.scale, 16, 0, out, lse, stream=s)
+    for prob in (pa, pb, pa):
+        bt.copy_(prob.block_table.cuda())
+        sl.copy_(prob.seq_lens.cuda())
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ref_out, ref_lse = oracle_gqa(prob)
+        compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out.reshape(out.shape),
+                ref_lse.reshape(lse.shape), what="graph replay")
+    assert pkv.check_counters(0) == 0
+
+
+def test_calls_on_two_streams_are_ordered():
+    prob = W.gqa_problem(20, 16, 64, 8, 16, "uniform", 1000, 8000, sinks=True)
+    q, kv, bt, sl, sk = (dev(prob.q), dev(prob.kv_cache), dev(prob.block_table),
+                         dev(prob.seq_lens), dev(prob.sinks))
+    outs = [torch.empty_like(q) for _ in range(4)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        pkv.paged_decode_attn(q, kv, bt, sl, sk, 0, prob.scale, 16, 0, o, None,
+                              stream=streams[i % 2])
+    torch.cuda.synchronize()
+    ref_out, _ = oracle_gqa(prob)
+    for o in outs:
+        assert np.max(np.abs(o.float().cpu().numpy().reshape(ref_out.shape) - ref_out)) <= TOL_OUT
+    assert pkv.check_counters(0) == 0
+
+
+# --------------------------------------------------------- input errors --
+
+def test_bad_block_table_entry_is_flagged_not_faulted():
+    prob = W.gqa_problem(21, 3, 8, 1, 16, "const", 100, 100)
+    bt = prob.block_table.clone()
+    nb = prob.kv_cache.shape[0]
+    bt[1, 2] = nb + 5          # past the end of the cache
+    bt[2, 0] = -1              # unassigned entry inside the attended range
+    q, kv, sl = dev(prob.q), dev(prob.kv_cache), dev(prob.seq_lens)
+    out = torch.empty_like(q)
+    pkv.paged_decode_attn(q, kv, bt.cuda(), sl, None, 0, prob.scale, 16, 0, out, None)
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.check_errors(0)
+    assert ei.value.code == -7
+    # the device stays usable and the next call is exact again
+    check(prob, what="after bad table")
+
+
+def test_seq_len_beyond_block_table_is_flagged():
+    prob = W.gqa_problem(22, 2, 8, 1, 16, "const", 64, 64, max_blocks=4)
+    sl = prob.seq_lens.clone()
+    sl[0] = 1000
+    out = torch.empty_like(dev(prob.q))
+    pkv.paged_decode_attn(dev(prob.q), dev(prob.kv_cache), dev(prob.block_table), sl.cuda(),
+                          None, 0, prob.scale, 16, 0, out, None)
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.check_errors(0)
+    assert ei.value.code == -7
+
+
+def test_capture_before_workspace_is_refused_message():
+    """Covered on the host: the first call allocates; an init during capture
+    is refused (the workspace already exists here, so init is a no-op)."""
+    pkv.init(0)  # idempotent
+    assert pkv.check_counters(0) == 0
+
+
+# ----------------------------------------------- full-size workloads ------
+
+@pytest.mark.parametrize("window", [0, 128])
+def test_flint_b64_full_size(window):
+    """B=64, Hq=64, Hkv=8, page 16, log-uniform lengths up to 32768, sinks:
+    every output row against the oracle, in the launch configuration the
+    benchmark times (library-chosen split cap)."""
+    prob = W.flint_gqa(0, window=window)
+    check(prob, what=f"flint W={window}")
+
+
+@pytest.mark.parametrize("cap", [1, 8, 32, 132])
+def test_long_context_b1_split_sweep(cap):
+    prob = _long(1)
+    out, lse = run_gqa(prob, cap)
+    ref_out, ref_lse = _long_ref(1)
+    compare(out, lse, ref_out.reshape(out.shape), ref_lse.reshape(lse.shape), what=f"long cap {cap}")
+    _long_outs.setdefault(1, []).append((out, lse))
+    if len(_long_outs[1]) > 1:
+        o0, l0 = _long_outs[1][0]
+        assert np.max(np.abs(out - o0)) <= 2e-3 and np.max(np.abs(lse - l0)) <= 1e-4
+
+
+_long_cache = {}
+_long_outs = {}
+
+
+def _long(B):
+    if B not in _long_cache:
+        _long_cache[B] = W.long_context(0, B=B)
+    return _long_cache[B]
+
+
+def _long_ref(B, rows=None):
+    key = (B, None if rows is None else tuple(rows))
+    if key not in _long_cache:
+        _long_cache[key] = oracle_gqa(_long(B), rows=rows)
+    return _long_cache[key]
+
+
+def test_long_context_b8_sampled_rows():
+    prob = _long(8)
+    rows = np.random.default_rng(0).choice(8 * 64, size=48, replace=False)
+    ref_out, ref_lse = _long_ref(8, rows)
+    prev = None
+    for cap in (132, 32):
+        out, lse = run_gqa(prob, cap)
+        o = out.reshape(-1, 128)[rows]
+        l = lse.reshape(-1)[rows]
+        compare(o, l, ref_out, ref_lse, what=f"long B=8 cap {cap}")
+        if prev is not None:
+            assert np.max(np.abs(out - prev[0])) <= 2e-3
+            assert np.max(np.abs(lse - prev[1])) <= 1e-4
+        prev = (out, lse)
+    _long_cache.clear()
