@@ -124,8 +124,9 @@ PKV_API int pkv_init(int device, size_t workspace_bytes);
  *   scale        softmax scale applied to q.k.
  *   page_size    P, tokens per page: 16 or 32 (must equal kv_cache.shape[2]).
  *   num_kv_splits static cap on the number of KV splits of one (request, kv
- *                head); 0 selects the library's cap.  Each request uses as
- *                many splits as its own length warrants, at most this many.
+ *                head); 0 selects the library's cap; values above 256 act as
+ *                256.  Each request uses as many splits as its own length
+ *                warrants (at least 256 keys per split), at most this many.
  *   out          bf16 [B, Hq, 128] (may not alias q); last dim contiguous.
  *   lse          fp32 [B, Hq] or NULL.
  *   stream       cudaStream_t (NULL = legacy default stream).

@@ -384,17 +384,17 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
   const pkv::Workspace& ws = st->ws;
 
   const int64_t item_bytes = int64_t(pkv::kGqaPartialFloats + pkv::kGqaMlFloats) * 4;
-  const int64_t max_items = int64_t(ws.partial_bytes) / item_bytes;
+  const int64_t max_items =
+      std::min<int64_t>(int64_t(ws.partial_bytes) / item_bytes, ws.num_counters - pkv::kTopCounters);
   const int64_t bh = B * Hkv;
-  if (bh > ws.num_counters)
+  if (bh > pkv::kTopCounters)
     return fail(PKV_ERR_WORKSPACE, "%lld (request, kv head) pairs exceed %lld counters",
-                (long long)bh, (long long)ws.num_counters);
-  int64_t cap = num_kv_splits;
-  if (cap == 0) {
-    cap = max_items / bh;
-    if (cap > 256) cap = 256;
-    if (cap < 1) cap = 1;
-  }
+                (long long)bh, (long long)pkv::kTopCounters);
+  // At most 256 splits per (request, kv head): the merge runs in at most two
+  // levels of at most 16 partials each.
+  int64_t cap = num_kv_splits == 0 ? max_items / bh : num_kv_splits;
+  if (cap > 256) cap = 256;
+  if (cap < 1) cap = 1;
   if (bh * cap > max_items)
     return fail(PKV_ERR_WORKSPACE, "workspace holds %lld split partials, %lld x %lld needed",
                 (long long)max_items, (long long)bh, (long long)cap);
@@ -407,7 +407,7 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
   const cuuint64_t gstride[3] = {cuuint64_t(kv_cache->stride[2]) * 2,
                                  cuuint64_t(kv_cache->stride[1]) * 2,
                                  cuuint64_t(kv_cache->stride[0]) * 2};
-  const cuuint32_t box[4] = {64, cuuint32_t(page_size), 1, 1};
+  const cuuint32_t box[4] = {64, 16, 1, 1};  // one 64-wide slice of a 16-token tile
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, kv_cache->data, gdim, gstride,
                        box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -439,14 +439,15 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
   p.scale_log2 = scale * 1.4426950408889634f;
   p.scale = scale;
   p.cap = int(cap);
-  p.min_pages = page_size == 16 ? 4 : 2;
-  const int64_t grid64 = std::min<int64_t>(ws.num_sms, bh * cap);
+  p.min_pages = 256 / page_size;  // a split streams at least 256 tokens (128 KB per kv head)
+  const int64_t grid64 = std::min<int64_t>(int64_t(ws.num_sms) * pkv::gqa_ctas_per_sm(), bh * cap);
   const int grid = int(grid64 < 1 ? 1 : grid64);
-  p.target_items = grid * 24;
+  p.target_items = grid * 12;
   p.part_o = ws.partials;
   p.part_ml = ws.partials + max_items * pkv::kGqaPartialFloats;
   p.max_items = max_items;
   p.counters = ws.counters;
+  p.group_counters = ws.counters + pkv::kTopCounters;
   p.sched = ws.sched;
   p.err = ws.err;
 

@@ -1,78 +1,81 @@
 // gqa_decode.cu -- split-KV paged GQA decode attention for sm_103a.
 //
 // Computes, for every request b and query head h (kv head h / 8),
-//   out = sum_j softmax_j(scale * q.k_j) v_j  with an optional sink logit in
-//   the denominator, lse = natural-log sum over keys of exp(scale * q.k_j),
+//   out = sum_j softmax_j(scale * q.k_j) v_j, with an optional sink logit in
+//   the denominator, and lse = log sum_j exp(scale * q.k_j) (keys only),
 // over keys [max(L - window, 0), L) gathered through block_table
 // ("vllm.models.flint.ops.decode_attention": flint_decode_attention and the
 // module's numerics paragraph; block-table indexing as in the transformers
 // "Atencion paginada" decode path).
 //
-// Design (one persistent CTA per SM, 1 producer warp + 8 consumer warps):
+// Design: persistent, two CTAs per SM, each 1 producer warp + 4 consumer warps.
 //  * Work items are (request, kv head, split) triples.  Every CTA derives the
 //    same item list in its prologue from seq_lens alone: request b's n_b
 //    attended pages are cut into s_b = min(cap, ceil(n_b / chunk)) contiguous
-//    splits, with chunk chosen from the total so that the launch has about
+//    page ranges, with chunk chosen from the total so that the launch has about
 //    target_items items (shorter requests use fewer splits).  CTAs pull items
-//    from a global queue (atomic head, reset by the last CTA to exit).
-//  * The producer warp reads block-table entries 32 at a time and streams each
-//    page of an item as four 128-byte-wide TMA tiles (K lo, K hi, V lo, V hi)
-//    with 128-byte swizzle into a 128 KB ring of page stages guarded by
-//    full/empty mbarriers; it runs ahead across item boundaries.
-//  * Consumer warp w handles pages w, w+8, ... of the item.  Per 16-token tile:
-//      S[8 heads x 16 tok] = Q K^T      mma.m16n8k16 (heads are the M side,
-//                                         rows 8..15 zero), K via ldmatrix
-//      online softmax in the exp2 domain (running max in unscaled logits),
-//      O^T[128 dims x 8 heads] += V^T P^T  mma.m16n8k16 with V via
-//                                         ldmatrix.trans and P^T taken
-//                                         straight from S's accumulator layout
-//    The 128-byte swizzle makes every ldmatrix phase conflict-free.
-//  * The 8 warps' (O, m, l) are merged through shared memory.  A single-split
-//    item writes out / lse directly; otherwise it publishes an fp32 partial and
-//    bumps the (request, kv head) arrival counter; the CTA that arrives last
-//    merges all partials and resets the counter to zero.
+//    from a global queue (atomic head, reset by the last CTA to exit), so the
+//    launch shape depends only on the device and the batch.
+//  * The producer warp bulk-copies the item's 8 query rows into a descriptor
+//    slot, reads block-table entries 32 at a time and streams every 16-token
+//    tile of every page as four 64-element TMA boxes (K lo, K hi, V lo, V hi)
+//    with 128-byte swizzle into an 8-stage ring (8 KB stages) guarded by
+//    full/empty mbarriers.  It runs ahead across item boundaries.
+//  * Consumer warp w takes tiles w, w+4, ... of the item.  It pulls the tile's
+//    K and V fragments into registers with ldmatrix (conflict-free thanks to
+//    the swizzle), frees the stage at once, then
+//      S[8 heads x 16 tok] = Q K^T          mma.m16n8k16, heads on the M side
+//                                             (rows 8..15 zero)
+//      online softmax, exp2 domain, running max in unscaled logits
+//      O^T[128 dims x 8 heads] += V^T P^T   mma.m16n8k16; P^T is S's
+//                                             accumulator layout rounded to bf16
+//  * The four warps' (O, m, l) merge in shared memory.  A single-split item
+//    writes out / lse directly.  Otherwise the fp32 partial is published and
+//    a per-group arrival counter (groups of up to 16 splits) is bumped with a
+//    release atomic; the last CTA of a group merges the group, and with more
+//    than one group the last group merges the group results.  Every counter is
+//    reset to zero by the CTA that consumed it.
 #include "pkv_internal.h"
 #include "ptx.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
-constexpr int kRingBytes = 128 * 1024;
+constexpr int kCtasPerSm = 2;
+constexpr int kStageBytes = 16 * 512;  // one 16-token tile: 16 x [K | V] x bf16
+constexpr int kStages = 8;
+constexpr int kBoxBytes = 16 * 128;    // one 64-element-wide TMA box of a tile
 constexpr int kItemSlots = 4;
-constexpr int kWbRow = 132;                                  // padded O row (floats)
+constexpr int kQBytes = kGqaGroup * kGqaHeadDim * 2;
+constexpr int kWbRow = 132;            // padded O row of the combine buffer (floats)
 constexpr int kWbFloats = kGqaGroup * kWbRow + 2 * kGqaGroup;  // O[8][132], m[8], l[8]
+constexpr int kMergeGroup = 16;        // splits merged by one CTA at the first level
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct ItemDesc {
   int item, b, kvh, split, nsplit, p0, p1, start_tok, L, seq_base, pad0, pad1;
 };
 
-template <int P>
-struct Cfg {
-  static constexpr int kStageBytes = P * 512;  // P tokens x [K | V] x bf16
-  static constexpr int kStages = kRingBytes / kStageBytes;
-  static constexpr int kTiles = P / 16;
-  static constexpr int kChunkBytes = P * 128;  // one 64-element-wide TMA tile
-  // shared-memory carve-up (offsets from a 1024-aligned base, 16-aligned)
-  static constexpr int kOffWbuf = kRingBytes;
-  static constexpr int kOffPrefix = kOffWbuf + kConsumerWarps * kWbFloats * 4;
-  static constexpr int kOffLens = kOffPrefix + ((kGqaMaxBatch + 1) * 4 + 15) / 16 * 16;
-  static constexpr int kOffItems = kOffLens + kGqaMaxBatch * 4;
-  static constexpr int kOffBars = kOffItems + kItemSlots * (int)sizeof(ItemDesc);
-  static constexpr int kNumBars = 2 * kStages + 2 * kItemSlots;
-  static constexpr int kOffMisc = kOffBars + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 64 + 1024;  // + alignment slack
-  static_assert(kOffWbuf % 16 == 0 && kOffPrefix % 16 == 0 && kOffLens % 16 == 0 &&
-                    kOffItems % 16 == 0 && kOffBars % 16 == 0 && kOffMisc % 16 == 0,
-                "shared-memory offsets must stay 16-byte aligned");
-  static_assert(kBytes <= 227 * 1024, "shared memory budget");
-};
+// shared-memory carve-up (offsets from a 1024-aligned base)
+constexpr int kOffWbuf = kStages * kStageBytes;
+constexpr int kOffQ = kOffWbuf + kConsumerWarps * kWbFloats * 4;
+constexpr int kOffPrefix = kOffQ + kItemSlots * kQBytes;
+constexpr int kOffItems = kOffPrefix + ((kGqaMaxBatch + 1) * 4 + 15) / 16 * 16;
+constexpr int kOffBars = kOffItems + kItemSlots * (int)sizeof(ItemDesc);
+constexpr int kNumBars = 2 * kStages + 2 * kItemSlots;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+static_assert(kOffWbuf % 1024 == 0 && kOffQ % 16 == 0 && kOffPrefix % 16 == 0 &&
+                  kOffItems % 16 == 0 && kOffBars % 16 == 0 && kOffMisc % 16 == 0,
+              "shared-memory offsets");
+static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(kMergeGroup * kGqaMlFloats <= kConsumerWarps * kWbFloats, "merge scratch");
 
-// Exclusive scan of one int per thread over the whole CTA; `scratch` holds
-// one int per warp plus one.  Returns the exclusive prefix; *total = sum.
+// Exclusive scan of one int per thread over the CTA; `scratch` holds one int
+// per warp plus one.  Returns the exclusive prefix; *total = the sum.
 __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
@@ -99,49 +102,107 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
   return res;
 }
 
-// Writes the final bf16 output row slice and lse of one (request, head).
-__device__ __forceinline__ void finalize(const GqaParams& p, int b, int head, int d4, float o0,
-                                         float o1, float o2, float o3, float m, float l,
-                                         bool write_lse) {
+template <int P>
+__device__ __forceinline__ int clamp_len(const GqaParams& p, int b) {
+  int L = __ldg(p.seq_lens + b);
+  if (L < 0) L = 0;
+  if (L > p.max_blocks * P) L = p.max_blocks * P;
+  return L;
+}
+
+__device__ __forceinline__ int window_start(const GqaParams& p, int L) {
+  return (p.window > 0 && L > p.window) ? L - p.window : 0;
+}
+
+// Out row slice [d0, d0 + 8) of one (request, head), and its lse.
+__device__ __forceinline__ void finalize(const GqaParams& p, int b, int head, int d0,
+                                         const float (&o)[8], float m, float l) {
   float inv = 0.f;
   if (l > 0.f) {
     float den = l;
-    if (p.sinks) den += ex2(__fmaf_rn(p.sinks[head], kLog2e, -m * p.scale_log2));
+    if (p.sinks) den += ex2(__fmaf_rn(__ldg(p.sinks + head), kLog2e, -m * p.scale_log2));
     inv = 1.f / den;
   }
-  uint2 v;
-  v.x = pack_bf16(o0 * inv, o1 * inv);
-  v.y = pack_bf16(o2 * inv, o3 * inv);
-  *reinterpret_cast<uint2*>(p.out + b * p.o_sb + head * p.o_sh + d4) = v;
-  if (write_lse && p.lse)
+  uint4 v;
+  v.x = pack_bf16(o[0] * inv, o[1] * inv);
+  v.y = pack_bf16(o[2] * inv, o[3] * inv);
+  v.z = pack_bf16(o[4] * inv, o[5] * inv);
+  v.w = pack_bf16(o[6] * inv, o[7] * inv);
+  *reinterpret_cast<uint4*>(p.out + b * p.o_sb + head * p.o_sh + d0) = v;
+  if (d0 == 0 && p.lse)
     p.lse[b * p.lse_sb + head * p.lse_sh] = (l > 0.f) ? m * p.scale + logf(l) : -INFINITY;
 }
 
+// Merge n published partials (slots slot0, slot0 + stride, ...) into
+// (o[8], M, L) for this thread's head eh and dims [ed, ed + 8).  `sml` is
+// shared scratch for n x 16 floats; all consumer threads take part.
+__device__ __forceinline__ void merge_slots(const GqaParams& p, long long slot0, int stride,
+                                            int n, float* sml, int eh, int ed, float (&o)[8],
+                                            float& M, float& Ls) {
+  const int ct = threadIdx.x;
+  for (int i = ct; i < n * kGqaMlFloats; i += kConsumers) {
+    const int s = i / kGqaMlFloats, k = i % kGqaMlFloats;
+    sml[i] = __ldcg(p.part_ml + (slot0 + (long long)s * stride) * kGqaMlFloats + k);
+  }
+  named_bar_sync(1, kConsumers);
+  M = -INFINITY;
+  for (int s = 0; s < n; ++s) M = fmaxf(M, sml[s * kGqaMlFloats + eh]);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = 0.f;
+  Ls = 0.f;
+  const float c2 = p.scale_log2;
+#pragma unroll 4
+  for (int s = 0; s < n; ++s) {
+    const float* src =
+        p.part_o + (slot0 + (long long)s * stride) * kGqaPartialFloats + eh * kGqaHeadDim + ed;
+    const float4 a = ldcg_f4(src), b = ldcg_f4(src + 4);
+    const float ms = sml[s * kGqaMlFloats + eh];
+    const float w = (ms == -INFINITY) ? 0.f : ex2((ms - M) * c2);
+    Ls = __fmaf_rn(w, sml[s * kGqaMlFloats + kGqaGroup + eh], Ls);
+    o[0] = __fmaf_rn(w, a.x, o[0]); o[1] = __fmaf_rn(w, a.y, o[1]);
+    o[2] = __fmaf_rn(w, a.z, o[2]); o[3] = __fmaf_rn(w, a.w, o[3]);
+    o[4] = __fmaf_rn(w, b.x, o[4]); o[5] = __fmaf_rn(w, b.y, o[5]);
+    o[6] = __fmaf_rn(w, b.z, o[6]); o[7] = __fmaf_rn(w, b.w, o[7]);
+  }
+}
+
+__device__ __forceinline__ void store_partial(const GqaParams& p, long long slot, int eh, int ed,
+                                              const float (&o)[8], float m, float l) {
+  float* dst = p.part_o + slot * kGqaPartialFloats + eh * kGqaHeadDim + ed;
+  *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
+  if (ed == 0) {
+    p.part_ml[slot * kGqaMlFloats + eh] = m;
+    p.part_ml[slot * kGqaMlFloats + kGqaGroup + eh] = l;
+  }
+}
+
 template <int P>
-__global__ void __launch_bounds__(kThreads, 1)
-    gqa_decode_kernel(const __grid_constant__ GqaParams p, const __grid_constant__ CUtensorMap kv_map) {
-  using C = Cfg<P>;
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    gqa_decode_kernel(const __grid_constant__ GqaParams p,
+                      const __grid_constant__ CUtensorMap kv_map) {
+  constexpr int TPP = P / 16;  // 16-token tiles per page
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
 
   const uint32_t ring = base_u32;
-  float* wbuf = reinterpret_cast<float*>(base + C::kOffWbuf);
-  int* prefix = reinterpret_cast<int*>(base + C::kOffPrefix);
-  int* lens = reinterpret_cast<int*>(base + C::kOffLens);
-  ItemDesc* items = reinterpret_cast<ItemDesc*>(base + C::kOffItems);
-  const uint32_t bars = base_u32 + C::kOffBars;
-  int* misc = reinterpret_cast<int*>(base + C::kOffMisc);
+  float* wbuf = reinterpret_cast<float*>(base + kOffWbuf);
+  const uint32_t qbuf = base_u32 + kOffQ;
+  int* prefix = reinterpret_cast<int*>(base + kOffPrefix);
+  ItemDesc* items = reinterpret_cast<ItemDesc*>(base + kOffItems);
+  const uint32_t bars = base_u32 + kOffBars;
+  int* misc = reinterpret_cast<int*>(base + kOffMisc);
   auto full_bar = [&](int s) { return bars + 8u * s; };
-  auto empty_bar = [&](int s) { return bars + 8u * (C::kStages + s); };
-  auto ifull_bar = [&](int s) { return bars + 8u * (2 * C::kStages + s); };
-  auto iempty_bar = [&](int s) { return bars + 8u * (2 * C::kStages + kItemSlots + s); };
+  auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+  auto ifull_bar = [&](int s) { return bars + 8u * (2 * kStages + s); };
+  auto iempty_bar = [&](int s) { return bars + 8u * (2 * kStages + kItemSlots + s); };
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (tid == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
@@ -154,55 +215,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumerWarps && lane == 0) tma_prefetch_desc(&kv_map);
 
   // ---- prologue: the item list, identical in every CTA -------------------
-  // pass 1: clamp lengths, count attended pages.
   const int B = p.B;
-  long long local_pages = 0;
+  int local_pages = 0;
   for (int b = tid; b < B; b += kThreads) {
-    int L = p.seq_lens[b];
-    if (L < 0) L = 0;
-    if ((long long)(L + P - 1) / P > p.max_blocks) {
-      atomicOr(p.err, DEVERR_SEQ_TOO_LONG);
-      L = p.max_blocks * P;
-    }
-    lens[b] = L;
-    const int start_tok = (p.window > 0 && L > p.window) ? L - p.window : 0;
-    local_pages += (L + P - 1) / P - start_tok / P;
+    const int raw = __ldg(p.seq_lens + b);
+    if ((long long)raw > (long long)p.max_blocks * P) atomicOr(p.err, DEVERR_SEQ_TOO_LONG);
+    const int L = clamp_len<P>(p, b);
+    local_pages += (L + P - 1) / P - window_start(p, L) / P;
   }
-  {
-    int lp = (int)local_pages;
-    int tot;
-    block_exclusive_scan(lp, misc, &tot);
-    local_pages = tot;
-  }
-  const long long total_pages = local_pages * p.Hkv;
-  int chunk = (int)((total_pages + p.target_items - 1) / p.target_items);
+  int total_pages;
+  block_exclusive_scan(local_pages, misc, &total_pages);
+  const long long total_ph = (long long)total_pages * p.Hkv;
+  int chunk = (int)((total_ph + p.target_items - 1) / p.target_items);
   if (chunk < p.min_pages) chunk = p.min_pages;
-  // pass 2: splits per request, exclusive prefix of items over requests.
   const int per = (B + kThreads - 1) / kThreads;
   const int b0 = tid * per;
   int my_items = 0;
-  for (int i = 0; i < per; ++i) {
-    const int b = b0 + i;
-    if (b >= B) break;
-    const int L = lens[b];
-    const int start_tok = (p.window > 0 && L > p.window) ? L - p.window : 0;
-    const int n = (L + P - 1) / P - start_tok / P;
-    int s = (n + chunk - 1) / chunk;
-    s = s < 1 ? 1 : (s > p.cap ? p.cap : s);
+  for (int i = 0; i < per && b0 + i < B; ++i) {
+    const int L = clamp_len<P>(p, b0 + i);
+    const int n = (L + P - 1) / P - window_start(p, L) / P;
+    const int s = max(1, min(p.cap, (n + chunk - 1) / chunk));
     my_items += s * p.Hkv;
   }
   int total_items;
   int run = block_exclusive_scan(my_items, misc, &total_items);
-  for (int i = 0; i < per; ++i) {
-    const int b = b0 + i;
-    if (b >= B) break;
-    prefix[b] = run;
-    const int L = lens[b];
-    const int start_tok = (p.window > 0 && L > p.window) ? L - p.window : 0;
-    const int n = (L + P - 1) / P - start_tok / P;
-    int s = (n + chunk - 1) / chunk;
-    s = s < 1 ? 1 : (s > p.cap ? p.cap : s);
-    run += s * p.Hkv;
+  for (int i = 0; i < per && b0 + i < B; ++i) {
+    prefix[b0 + i] = run;
+    const int L = clamp_len<P>(p, b0 + i);
+    const int n = (L + P - 1) / P - window_start(p, L) / P;
+    run += max(1, min(p.cap, (n + chunk - 1) / chunk)) * p.Hkv;
   }
   if (tid == 0) prefix[B] = total_items;
   if ((long long)total_items > p.max_items) {
@@ -212,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 
   if (warp == kConsumerWarps) {
-    // ===================== producer warp =====================
+    // =========================== producer warp ===========================
     int next = 0;
     if (lane == 0) next = atomicAdd(&p.sched[0], 1);
     next = __shfl_sync(0xffffffffu, next, 0);
@@ -224,8 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         next = __shfl_sync(0xffffffffu, next, 0);
       }
       const int slot = it % kItemSlots;
-      const uint32_t par = (it / kItemSlots) & 1;
-      if (lane == 0) mbar_wait(iempty_bar(slot), par ^ 1u, p.err);
+      if (lane == 0) mbar_wait(iempty_bar(slot), ((it / kItemSlots) & 1) ^ 1u, p.err);
       __syncwarp();
       if (item >= total_items) {
         if (lane == 0) {
@@ -234,8 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         break;
       }
-      // decode: request = last b with prefix[b] <= item
-      int lo = 0, hi = B - 1;
+      int lo = 0, hi = B - 1;  // request = last b with prefix[b] <= item
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
@@ -244,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nsplit = (prefix[b + 1] - prefix[b]) / p.Hkv;
       const int local = item - prefix[b];
       const int kvh = local / nsplit, split = local % nsplit;
-      const int L = lens[b];
-      const int start_tok = (p.window > 0 && L > p.window) ? L - p.window : 0;
+      const int L = clamp_len<P>(p, b);
+      const int start_tok = window_start(p, L);
       const int sp = start_tok / P;
       const int n = (L + P - 1) / P - sp;
       const int p0 = sp + (int)((long long)n * split / nsplit);
@@ -254,7 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ItemDesc& d = items[slot];
         d.item = item; d.b = b; d.kvh = kvh; d.split = split; d.nsplit = nsplit;
         d.p0 = p0; d.p1 = p1; d.start_tok = start_tok; d.L = L; d.seq_base = (int)seq;
-        mbar_arrive(ifull_bar(slot));  // release: the descriptor is visible to waiters
+        // the descriptor stores are released by this arrive; the phase also
+        // waits for the 8 query rows
+        mbar_arrive_expect_tx(ifull_bar(slot), kQBytes);
+        const uint16_t* qrow = p.q + b * p.q_sb + (long long)(kvh * kGqaGroup) * p.q_sh;
+#pragma unroll
+        for (int h = 0; h < kGqaGroup; ++h)
+          bulk_load(qbuf + slot * kQBytes + h * kGqaHeadDim * 2, qrow + h * p.q_sh,
+                    kGqaHeadDim * 2, ifull_bar(slot));
       }
       const int32_t* bt_row = p.bt + (long long)b * p.bt_sb;
       for (int pb = p0; pb < p1; pb += 32) {
@@ -266,32 +312,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < cnt; ++i) {
           const int blk_i = __shfl_sync(0xffffffffu, blk, i);
-          if (lane == 0) {
-            const int stage = seq % C::kStages;
-            const uint32_t ph = (seq / C::kStages) & 1;
-            mbar_wait(empty_bar(stage), ph ^ 1u, p.err);
-            mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
-            const uint32_t dst = ring + stage * C::kStageBytes;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              tma_load_4d(dst + c * C::kChunkBytes, &kv_map, full_bar(stage), 64 * c, 0, kvh, blk_i);
+          for (int sub = 0; sub < TPP; ++sub) {
+            if (lane == 0) {
+              const int stage = seq % kStages;
+              mbar_wait(empty_bar(stage), ((seq / kStages) & 1) ^ 1u, p.err);
+              mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+              const uint32_t dst = ring + stage * kStageBytes;
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                tma_load_4d(dst + c * kBoxBytes, &kv_map, full_bar(stage), 64 * c, 16 * sub, kvh,
+                            blk_i);
+            }
+            ++seq;
           }
-          ++seq;
         }
       }
     }
-    // Every issued copy has landed before the CTA may exit (the consumers
-    // waited on them already unless a wait gave up).
     if (lane == 0) {
-      const uint32_t n_recent = seq < (uint32_t)C::kStages ? seq : (uint32_t)C::kStages;
-      for (uint32_t k = seq - n_recent; k < seq; ++k)
-        mbar_wait(full_bar(k % C::kStages), (k / C::kStages) & 1, p.err);
-    }
-    // last CTA out resets the queue for the next launch
-    if (lane == 0) {
+      // every issued copy has landed before the CTA may exit (the consumers
+      // waited on them already unless a wait gave up)
+      const uint32_t recent = seq < (uint32_t)kStages ? seq : (uint32_t)kStages;
+      for (uint32_t k = seq - recent; k < seq; ++k)
+        mbar_wait(full_bar(k % kStages), (k / kStages) & 1, p.err);
+      // the last CTA out resets the queue for the next launch
       __threadfence();
-      const int old = atomicAdd(&p.sched[1], 1);
-      if (old == (int)gridDim.x - 1) {
+      if (atomicAdd(&p.sched[1], 1) == (int)gridDim.x - 1) {
         atomicExch(&p.sched[0], 0);
         atomicExch(&p.sched[1], 0);
       }
@@ -299,123 +345,129 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  // ======================= consumer warps =======================
+  // ============================ consumer warps ============================
   const int g = lane >> 2, t = lane & 3;
-  // ldmatrix lane addressing: matrix mi = lane / 8 supplies row r = lane % 8;
-  // matrices 0,1: tile rows 0..7; 2,3: rows 8..15; odd matrices: the upper
-  // 8 elements (next 16-byte unit) of a 16-element k-step.
+  // ldmatrix addressing: matrix mi = lane / 8 supplies row r = lane % 8 of
+  // tile rows 0..7 (mi = 0, 1) or 8..15 (mi = 2, 3); odd mi read the upper
+  // 16-byte unit of a 16-element k-step.  The 128-byte swizzle XORs the unit
+  // index with the row index mod 8.
   const int mi = lane >> 3, r = lane & 7;
   const uint32_t row_off = (uint32_t)(r + 8 * (mi >> 1)) * 128u;
   const int ubit = mi & 1;
   float* my_wb = wbuf + warp * kWbFloats;
-  const int ct = tid;  // consumer thread index 0..255
-  const int eh = ct >> 5, ed = (ct & 31) * 4;  // epilogue: head, first of 4 dims
+  const int eh = tid >> 4, ed = (tid & 15) * 8;  // epilogue: head, first of 8 dims
+  const float c2 = p.scale_log2;
 
   for (int it = 0;; ++it) {
     const int slot = it % kItemSlots;
     mbar_wait(ifull_bar(slot), (it / kItemSlots) & 1, p.err);
     const ItemDesc d = items[slot];
+    // Q as the A operand: rows = the 8 heads of this kv head (rows 8..15 zero)
+    uint32_t qa[8][2];
+    if (d.item >= 0) {
+      const uint8_t* qs = base + kOffQ + slot * kQBytes + g * kGqaHeadDim * 2;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        qa[s][0] = *reinterpret_cast<const uint32_t*>(qs + (16 * s + 2 * t) * 2);
+        qa[s][1] = *reinterpret_cast<const uint32_t*>(qs + (16 * s + 8 + 2 * t) * 2);
+      }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(iempty_bar(slot));
     if (d.item < 0) break;
 
-    // Q as the A operand (rows = the 8 heads of this kv head; rows 8..15 zero).
-    uint32_t qa[8][2];
-    {
-      const uint16_t* qrow = p.q + d.b * p.q_sb + (d.kvh * kGqaGroup + g) * p.q_sh;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        qa[s][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * s + 2 * t));
-        qa[s][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * s + 8 + 2 * t));
-      }
-    }
     float acc[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
     float m = -INFINITY, l = 0.f;
-    const float c2 = p.scale_log2;
 
-    const int npages = d.p1 - d.p0;
-    for (int k = warp; k < npages; k += kConsumerWarps) {
+    const int ntiles = (d.p1 - d.p0) * TPP;
+    for (int k = warp; k < ntiles; k += kConsumerWarps) {
       const uint32_t seq = (uint32_t)d.seq_base + (uint32_t)k;
-      const int stage = seq % C::kStages;
-      mbar_wait(full_bar(stage), (seq / C::kStages) & 1, p.err);
-      const uint32_t st = ring + stage * C::kStageBytes;
-      const int page = d.p0 + k;
+      const int stage = seq % kStages;
+      mbar_wait(full_bar(stage), (seq / kStages) & 1, p.err);
+      const uint32_t tile = ring + stage * kStageBytes + row_off;
+      // K fragments (B operand of S = Q K^T) and V fragments (A operand of
+      // O^T += V^T P^T) for the whole tile, then the stage is released.
+      uint32_t kf[8][4], vf[8][4];
 #pragma unroll
-      for (int u = 0; u < C::kTiles; ++u) {
-        const int tok0 = page * P + 16 * u;
-        const uint32_t tile = st + 16u * u * 128u + row_off;
-        // ---- S = Q K^T over 128 dims: 4 independent accumulator chains ----
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-        float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t unit = (uint32_t)((2 * (s & 3) + ubit) ^ r);
+        ldsm_x4(tile + (s >> 2) * kBoxBytes + (unit << 4), kf[s][0], kf[s][1], kf[s][2], kf[s][3]);
+      }
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const uint32_t unit = (uint32_t)((2 * (s & 3) + ubit) ^ r);
-          uint32_t k0, k1, k2, k3;
-          ldsm_x4(tile + (s >> 2) * C::kChunkBytes + (unit << 4), k0, k1, k2, k3);
-          if (s & 1) {
-            mma_bf16_16816(sb, qa[s][0], 0u, qa[s][1], 0u, k0, k1);
-            mma_bf16_16816(sd, qa[s][0], 0u, qa[s][1], 0u, k2, k3);
-          } else {
-            mma_bf16_16816(sa, qa[s][0], 0u, qa[s][1], 0u, k0, k1);
-            mma_bf16_16816(sc, qa[s][0], 0u, qa[s][1], 0u, k2, k3);
-          }
-        }
-        // lane (g, t): head g, tile tokens 2t, 2t+1 (x0, x1) and 8+2t, 9+2t (x2, x3)
-        float x0 = sa[0] + sb[0], x1 = sa[1] + sb[1];
-        float x2 = sc[0] + sd[0], x3 = sc[1] + sd[1];
-        const int pa = tok0 + 2 * t;
-        const bool v0 = pa >= d.start_tok && pa < d.L;
-        const bool v1 = pa + 1 >= d.start_tok && pa + 1 < d.L;
-        const bool v2 = pa + 8 >= d.start_tok && pa + 8 < d.L;
-        const bool v3 = pa + 9 >= d.start_tok && pa + 9 < d.L;
-        x0 = v0 ? x0 : -INFINITY;
-        x1 = v1 ? x1 : -INFINITY;
-        x2 = v2 ? x2 : -INFINITY;
-        x3 = v3 ? x3 : -INFINITY;
-        // ---- online softmax (exp2 domain, running max in raw logits) ----
-        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mn = fmaxf(m, mx);
-        const float msc = (mn == -INFINITY) ? 0.f : mn * c2;
-        const float alpha = ex2(__fmaf_rn(m, c2, -msc));
-        const float e0 = ex2(__fmaf_rn(x0, c2, -msc));
-        const float e1 = ex2(__fmaf_rn(x1, c2, -msc));
-        const float e2 = ex2(__fmaf_rn(x2, c2, -msc));
-        const float e3 = ex2(__fmaf_rn(x3, c2, -msc));
-        l = __fmaf_rn(l, alpha, (e0 + e1) + (e2 + e3));
-        m = mn;
-        // O^T columns are heads 2t, 2t+1: fetch their rescale factors
-        const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
-        const float al1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          acc[j][0] *= al0; acc[j][1] *= al1; acc[j][2] *= al0; acc[j][3] *= al1;
-        }
-        // P^T as the B operand: exactly S's accumulator pairs, rounded to bf16
-        const uint32_t pb0 = pack_bf16(e0, e1), pb1 = pack_bf16(e2, e3);
-        // V rows outside [start_tok, L) are zeroed: stale cache contents
-        // (NaN, Inf) must not reach P.V even with P = 0.
-        const bool edge = (tok0 < d.start_tok) || (tok0 + 16 > d.L);
-        const uint32_t mlo = (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
-        const uint32_t mhi = (v2 ? 0x0000ffffu : 0u) | (v3 ? 0xffff0000u : 0u);
-        // ---- O^T += V^T P^T: 8 m-tiles of 16 dims ----
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t unit = (uint32_t)((2 * (j & 3) + ubit) ^ r);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(tile + (2 + (j >> 2)) * C::kChunkBytes + (unit << 4), a0, a1, a2, a3);
-          if (edge) { a0 &= mlo; a1 &= mlo; a2 &= mhi; a3 &= mhi; }
-          mma_bf16_16816(acc[j], a0, a1, a2, a3, pb0, pb1);
-        }
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t unit = (uint32_t)((2 * (j & 3) + ubit) ^ r);
+        ldsm_x4_trans(tile + (2 + (j >> 2)) * kBoxBytes + (unit << 4), vf[j][0], vf[j][1],
+                      vf[j][2], vf[j][3]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(stage));
+
+      const int tok0 = (d.p0 + k / TPP) * P + 16 * (k % TPP);
+      // ---- S = Q K^T over 128 dims, 4 independent accumulator chains ----
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        if (s & 1) {
+          mma_bf16_16816(sb, qa[s][0], 0u, qa[s][1], 0u, kf[s][0], kf[s][1]);
+          mma_bf16_16816(sd, qa[s][0], 0u, qa[s][1], 0u, kf[s][2], kf[s][3]);
+        } else {
+          mma_bf16_16816(sa, qa[s][0], 0u, qa[s][1], 0u, kf[s][0], kf[s][1]);
+          mma_bf16_16816(sc, qa[s][0], 0u, qa[s][1], 0u, kf[s][2], kf[s][3]);
+        }
+      }
+      // lane (g, t): head g; tile tokens 2t, 2t+1 (x0, x1) and 8+2t, 9+2t (x2, x3)
+      float x0 = sa[0] + sb[0], x1 = sa[1] + sb[1];
+      float x2 = sc[0] + sd[0], x3 = sc[1] + sd[1];
+      const int pa = tok0 + 2 * t;
+      const bool v0 = pa >= d.start_tok && pa < d.L;
+      const bool v1 = pa + 1 >= d.start_tok && pa + 1 < d.L;
+      const bool v2 = pa + 8 >= d.start_tok && pa + 8 < d.L;
+      const bool v3 = pa + 9 >= d.start_tok && pa + 9 < d.L;
+      x0 = v0 ? x0 : -INFINITY;
+      x1 = v1 ? x1 : -INFINITY;
+      x2 = v2 ? x2 : -INFINITY;
+      x3 = v3 ? x3 : -INFINITY;
+      // ---- online softmax (exp2 domain, running max in raw logits) ----
+      float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float mn = fmaxf(m, mx);
+      const float msc = (mn == -INFINITY) ? 0.f : mn * c2;
+      const float alpha = ex2(__fmaf_rn(m, c2, -msc));
+      const float e0 = ex2(__fmaf_rn(x0, c2, -msc));
+      const float e1 = ex2(__fmaf_rn(x1, c2, -msc));
+      const float e2 = ex2(__fmaf_rn(x2, c2, -msc));
+      const float e3 = ex2(__fmaf_rn(x3, c2, -msc));
+      l = __fmaf_rn(l, alpha, (e0 + e1) + (e2 + e3));
+      m = mn;
+      // O^T columns are heads 2t, 2t+1: their rescale factors live on lanes 8t, 8t+4
+      const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
+      const float al1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc[j][0] *= al0; acc[j][1] *= al1; acc[j][2] *= al0; acc[j][3] *= al1;
+      }
+      const uint32_t pb0 = pack_bf16(e0, e1), pb1 = pack_bf16(e2, e3);
+      // V rows outside [start_tok, L) are zeroed: stale cache contents (NaN,
+      // Inf) must not reach P.V even with P = 0.
+      if ((tok0 < d.start_tok) || (tok0 + 16 > d.L)) {
+        const uint32_t mlo = (v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u);
+        const uint32_t mhi = (v2 ? 0x0000ffffu : 0u) | (v3 ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          vf[j][0] &= mlo; vf[j][1] &= mlo; vf[j][2] &= mhi; vf[j][3] &= mhi;
+        }
+      }
+      // ---- O^T += V^T P^T: 8 m-tiles of 16 dims ----
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        mma_bf16_16816(acc[j], vf[j][0], vf[j][1], vf[j][2], vf[j][3], pb0, pb1);
     }
 
-    // ---- merge the 8 warps' (O, m, l) through shared memory ----
+    // ---- merge the warps' (O, m, l) in shared memory ----
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
 #pragma unroll
@@ -435,77 +487,78 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w)
       mc = fmaxf(mc, wbuf[w * kWbFloats + kGqaGroup * kWbRow + eh]);
-    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f, lc = 0.f;
+    float o[8], lc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
       const float* wb = wbuf + w * kWbFloats;
       const float mw = wb[kGqaGroup * kWbRow + eh];
       const float cw = (mw == -INFINITY) ? 0.f : ex2((mw - mc) * c2);
       lc = __fmaf_rn(cw, wb[kGqaGroup * kWbRow + kGqaGroup + eh], lc);
-      const float4 ov = *reinterpret_cast<const float4*>(wb + eh * kWbRow + ed);
-      o0 = __fmaf_rn(cw, ov.x, o0); o1 = __fmaf_rn(cw, ov.y, o1);
-      o2 = __fmaf_rn(cw, ov.z, o2); o3 = __fmaf_rn(cw, ov.w, o3);
+      const float4 a = *reinterpret_cast<const float4*>(wb + eh * kWbRow + ed);
+      const float4 bq = *reinterpret_cast<const float4*>(wb + eh * kWbRow + ed + 4);
+      o[0] = __fmaf_rn(cw, a.x, o[0]); o[1] = __fmaf_rn(cw, a.y, o[1]);
+      o[2] = __fmaf_rn(cw, a.z, o[2]); o[3] = __fmaf_rn(cw, a.w, o[3]);
+      o[4] = __fmaf_rn(cw, bq.x, o[4]); o[5] = __fmaf_rn(cw, bq.y, o[5]);
+      o[6] = __fmaf_rn(cw, bq.z, o[6]); o[7] = __fmaf_rn(cw, bq.w, o[7]);
     }
     const int head = d.kvh * kGqaGroup + eh;
     if (d.nsplit == 1) {
-      finalize(p, d.b, head, ed, o0, o1, o2, o3, mc, lc, ed == 0);
+      finalize(p, d.b, head, ed, o, mc, lc);
     } else {
-      float* po = p.part_o + (long long)d.item * kGqaPartialFloats + eh * kGqaHeadDim + ed;
-      *reinterpret_cast<float4*>(po) = make_float4(o0, o1, o2, o3);
-      if (ed == 0) {
-        p.part_ml[(long long)d.item * kGqaMlFloats + eh] = mc;
-        p.part_ml[(long long)d.item * kGqaMlFloats + kGqaGroup + eh] = lc;
-      }
-      __threadfence();
+      // publish this split, then count arrivals in its group of <= 16 splits
+      store_partial(p, d.item, eh, ed, o, mc, lc);
+      const long long first = d.item - d.split;
+      const int gi = d.split / kMergeGroup;
+      const long long gfirst = first + gi * kMergeGroup;
+      const int gsize = min(kMergeGroup, d.nsplit - gi * kMergeGroup);
+      const int ngroups = (d.nsplit + kMergeGroup - 1) / kMergeGroup;
+      int* gcnt = p.group_counters + gfirst;
       named_bar_sync(1, kConsumers);
-      int* counter = p.counters + d.b * p.Hkv + d.kvh;
-      if (ct == 0) misc[8] = atomicAdd(counter, 1);
+      if (tid == 0) misc[12] = atomic_add_acq_rel_gpu(gcnt, 1);
       named_bar_sync(1, kConsumers);
-      if (misc[8] == d.nsplit - 1) {
-        __threadfence();
-        const long long first = d.item - d.split;
-        float M = -INFINITY;
-        for (int s = 0; s < d.nsplit; ++s)
-          M = fmaxf(M, __ldcg(p.part_ml + (first + s) * kGqaMlFloats + eh));
-        o0 = o1 = o2 = o3 = 0.f;
-        float Ls = 0.f;
-#pragma unroll 4
-        for (int s = 0; s < d.nsplit; ++s) {
-          const float ms = __ldcg(p.part_ml + (first + s) * kGqaMlFloats + eh);
-          const float ls = __ldcg(p.part_ml + (first + s) * kGqaMlFloats + kGqaGroup + eh);
-          const float4 ov = ldcg_f4(p.part_o + (first + s) * kGqaPartialFloats + eh * kGqaHeadDim + ed);
-          const float w = (ms == -INFINITY) ? 0.f : ex2((ms - M) * c2);
-          Ls = __fmaf_rn(w, ls, Ls);
-          o0 = __fmaf_rn(w, ov.x, o0); o1 = __fmaf_rn(w, ov.y, o1);
-          o2 = __fmaf_rn(w, ov.z, o2); o3 = __fmaf_rn(w, ov.w, o3);
+      if (misc[12] == gsize - 1) {
+        float M, Ls;
+        merge_slots(p, gfirst, 1, gsize, wbuf, eh, ed, o, M, Ls);
+        if (tid == 0) store_relaxed_gpu(gcnt, 0);
+        if (ngroups == 1) {
+          finalize(p, d.b, head, ed, o, M, Ls);
+        } else {
+          store_partial(p, gfirst, eh, ed, o, M, Ls);  // the group result
+          int* tcnt = p.counters + d.b * p.Hkv + d.kvh;
+          named_bar_sync(1, kConsumers);
+          if (tid == 0) misc[13] = atomic_add_acq_rel_gpu(tcnt, 1);
+          named_bar_sync(1, kConsumers);
+          if (misc[13] == ngroups - 1) {
+            merge_slots(p, first, kMergeGroup, ngroups, wbuf, eh, ed, o, M, Ls);
+            if (tid == 0) store_relaxed_gpu(tcnt, 0);
+            finalize(p, d.b, head, ed, o, M, Ls);
+          }
         }
-        finalize(p, d.b, head, ed, o0, o1, o2, o3, M, Ls, ed == 0);
-        if (ct == 0) *counter = 0;  // self-reset for the next launch
       }
     }
-    named_bar_sync(1, kConsumers);  // wbuf and misc[8] are reused by the next item
+    named_bar_sync(1, kConsumers);  // wbuf and misc are reused by the next item
   }
+}
+
+template <int P>
+cudaError_t launch_page(const GqaParams& p, const CUtensorMap& kv_map, int grid,
+                        cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        gqa_decode_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  gqa_decode_kernel<P><<<grid, kThreads, kSmemBytes, stream>>>(p, kv_map);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t gqa_smem_bytes(int page_size) {
-  return page_size == 16 ? Cfg<16>::kBytes : Cfg<32>::kBytes;
-}
-
-template <int P>
-static cudaError_t launch_page(const GqaParams& p, const CUtensorMap& kv_map, int grid,
-                               cudaStream_t stream) {
-  static bool attr_set = false;  // per process; the attribute is per device function
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        gqa_decode_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<P>::kBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  gqa_decode_kernel<P><<<grid, kThreads, Cfg<P>::kBytes, stream>>>(p, kv_map);
-  return cudaGetLastError();
-}
+int gqa_ctas_per_sm() { return kCtasPerSm; }
 
 cudaError_t launch_gqa_decode(const GqaParams& p, const CUtensorMap& kv_map, int page_size,
                               int grid, cudaStream_t stream) {

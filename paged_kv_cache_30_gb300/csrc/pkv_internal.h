@@ -59,7 +59,8 @@ struct GqaParams {
   float* part_o;       // [max_items][8][128]
   float* part_ml;      // [max_items][16]
   int64_t max_items;
-  int* counters;       // [B * Hkv]
+  int* counters;       // [B * Hkv] arrival counters of the last merge level
+  int* group_counters; // [max_items] arrival counters of split groups (by first item)
   int* sched;
   int* err;
 };
@@ -67,6 +68,10 @@ struct GqaParams {
 // Launch the GQA decode kernel for page size 16 or 32 on `grid` CTAs.
 cudaError_t launch_gqa_decode(const GqaParams& p, const CUtensorMap& kv_map, int page_size,
                               int grid, cudaStream_t stream);
-size_t gqa_smem_bytes(int page_size);
+int gqa_ctas_per_sm();
+
+// The counter region of the workspace holds 2^20 ints: the first half for
+// (request, kv head) counters, the second half for split-group counters.
+constexpr int64_t kTopCounters = int64_t(1) << 19;
 
 }  // namespace pkv
