@@ -43,19 +43,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier, giving up after ~2^31 SM cycles
-// (about a second): the error bit is set and the caller carries on, so a
-// broken pipeline ends the kernel with an error status instead of hanging.
-// Once any wait of the launch has given up, later waits that do not complete
-// at once return immediately, so the kernel drains quickly.
+// Wait for phase `parity` of an mbarrier.  The wait gives up after ~2^31 SM
+// cycles (about a second): the error bit is set and the caller carries on, so
+// a broken pipeline ends the kernel with an error status instead of hanging.
+// A wait that has already lasted ~2^20 cycles also checks whether another wait
+// of the launch gave up, and if so returns at once, so the kernel drains
+// quickly.  The fast path touches no global memory.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
-  if (*reinterpret_cast<volatile int*>(err) & DEVERR_WAIT_TIMEOUT) return false;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > (1ll << 31)) {
-      atomicOr(err, DEVERR_WAIT_TIMEOUT);
-      return false;
+    const long long dt = clock64() - t0;
+    if (dt > (1ll << 20)) {
+      if (*reinterpret_cast<volatile int*>(err) & DEVERR_WAIT_TIMEOUT) return false;
+      if (dt > (1ll << 31)) {
+        atomicOr(err, DEVERR_WAIT_TIMEOUT);
+        return false;
+      }
     }
   }
   return true;
