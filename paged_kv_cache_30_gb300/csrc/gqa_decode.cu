@@ -63,14 +63,13 @@ struct ItemDesc {
 constexpr int kOffWbuf = kStages * kStageBytes;
 constexpr int kOffQ = kOffWbuf + kConsumerWarps * kWbFloats * 4;
 constexpr int kOffPrefix = kOffQ + kItemSlots * kQBytes;
-constexpr int kOffLens = kOffPrefix + ((kGqaMaxBatch + 1) * 4 + 15) / 16 * 16;
-constexpr int kOffItems = kOffLens + kGqaMaxBatch * 4;
+constexpr int kOffItems = kOffPrefix + ((kGqaMaxBatch + 1) * 4 + 15) / 16 * 16;
 constexpr int kOffBars = kOffItems + kItemSlots * (int)sizeof(ItemDesc);
 constexpr int kNumBars = 2 * kStages + 2 * kItemSlots;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 static_assert(kOffWbuf % 1024 == 0 && kOffQ % 16 == 0 && kOffPrefix % 16 == 0 &&
-                  kOffLens % 16 == 0 && kOffItems % 16 == 0 && kOffBars % 16 == 0 && kOffMisc % 16 == 0,
+                  kOffItems % 16 == 0 && kOffBars % 16 == 0 && kOffMisc % 16 == 0,
               "shared-memory offsets");
 static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 static_assert(kMergeGroup * kGqaMlFloats <= kConsumerWarps * kWbFloats, "merge scratch");
@@ -113,41 +112,6 @@ __device__ __forceinline__ int clamp_len(const GqaParams& p, int b) {
 
 __device__ __forceinline__ int window_start(const GqaParams& p, int L) {
   return (p.window > 0 && L > p.window) ? L - p.window : 0;
-}
-
-struct ItemInfo {
-  int b, kvh, split, nsplit, p0, p1, start_tok, L;
-};
-
-// Which (request, kv head, split) an item index names, and its page range.
-template <int P>
-__device__ __forceinline__ ItemInfo decode_item(const GqaParams& p, const int* prefix,
-                                                const int* lens, int item) {
-  int lo = 0, hi = p.B - 1;  // request = last b with prefix[b] <= item
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
-  }
-  ItemInfo r;
-  r.b = lo;
-  r.nsplit = (prefix[lo + 1] - prefix[lo]) / p.Hkv;
-  const int local = item - prefix[lo];
-  r.kvh = local / r.nsplit;
-  r.split = local % r.nsplit;
-  r.L = lens[lo];
-  r.start_tok = window_start(p, r.L);
-  const int sp = r.start_tok / P;
-  const int n = (r.L + P - 1) / P - sp;
-  r.p0 = sp + (int)((long long)n * r.split / r.nsplit);
-  r.p1 = sp + (int)((long long)n * (r.split + 1) / r.nsplit);
-  return r;
-}
-
-// Block-table entries [from, from + 32) of request b (lane i holds entry
-// from + i), bounded by `end`.
-__device__ __forceinline__ int load_bt_chunk(const GqaParams& p, int b, int from, int end,
-                                             int lane) {
-  return (from + lane < end) ? __ldg(p.bt + (long long)b * p.bt_sb + from + lane) : 0;
 }
 
 // Out row slice [d0, d0 + 8) of one (request, head), and its lse.
@@ -227,7 +191,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   float* wbuf = reinterpret_cast<float*>(base + kOffWbuf);
   const uint32_t qbuf = base_u32 + kOffQ;
   int* prefix = reinterpret_cast<int*>(base + kOffPrefix);
-  int* lens = reinterpret_cast<int*>(base + kOffLens);
   ItemDesc* items = reinterpret_cast<ItemDesc*>(base + kOffItems);
   const uint32_t bars = base_u32 + kOffBars;
   int* misc = reinterpret_cast<int*>(base + kOffMisc);
@@ -258,7 +221,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int raw = __ldg(p.seq_lens + b);
     if ((long long)raw > (long long)p.max_blocks * P) atomicOr(p.err, DEVERR_SEQ_TOO_LONG);
     const int L = clamp_len<P>(p, b);
-    lens[b] = L;
     local_pages += (L + P - 1) / P - window_start(p, L) / P;
   }
   int total_pages;
@@ -270,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const int b0 = tid * per;
   int my_items = 0;
   for (int i = 0; i < per && b0 + i < B; ++i) {
-    const int L = lens[b0 + i];
+    const int L = clamp_len<P>(p, b0 + i);
     const int n = (L + P - 1) / P - window_start(p, L) / P;
     const int s = max(1, min(p.cap, (n + chunk - 1) / chunk));
     my_items += s * p.Hkv;
@@ -279,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   int run = block_exclusive_scan(my_items, misc, &total_items);
   for (int i = 0; i < per && b0 + i < B; ++i) {
     prefix[b0 + i] = run;
-    const int L = lens[b0 + i];
+    const int L = clamp_len<P>(p, b0 + i);
     const int n = (L + P - 1) / P - window_start(p, L) / P;
     run += max(1, min(p.cap, (n + chunk - 1) / chunk)) * p.Hkv;
   }
@@ -292,60 +254,62 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   if (warp == kConsumerWarps) {
     // =========================== producer warp ===========================
-    // Latency hiding: the queue index of the item after the current one is
-    // fetched one item ahead, and the block-table chunk needed next (this
-    // item's next 32 pages, or the next item's first 32) is loaded while the
-    // current chunk's tiles are issued.
-    int cur = 0, nxt = 0;
-    if (lane == 0) {
-      cur = atomicAdd(&p.sched[0], 1);
-      nxt = atomicAdd(&p.sched[0], 1);
-    }
-    cur = __shfl_sync(0xffffffffu, cur, 0);
-    ItemInfo ci = {};
-    int blk_pref = 0;
-    if (cur < total_items) {
-      ci = decode_item<P>(p, prefix, lens, cur);
-      blk_pref = load_bt_chunk(p, ci.b, ci.p0, ci.p1, lane);
-    }
+    int next = 0;
+    if (lane == 0) next = atomicAdd(&p.sched[0], 1);
+    next = __shfl_sync(0xffffffffu, next, 0);
     uint32_t seq = 0;
     for (int it = 0;; ++it) {
+      const int item = next;
+      if (item < total_items) {
+        if (lane == 0) next = atomicAdd(&p.sched[0], 1);
+        next = __shfl_sync(0xffffffffu, next, 0);
+      }
       const int slot = it % kItemSlots;
       if (lane == 0) mbar_wait(iempty_bar(slot), ((it / kItemSlots) & 1) ^ 1u, p.err);
       __syncwarp();
-      if (cur >= total_items) {
+      if (item >= total_items) {
         if (lane == 0) {
           items[slot].item = -1;
           mbar_arrive(ifull_bar(slot));
         }
         break;
       }
+      int lo = 0, hi = B - 1;  // request = last b with prefix[b] <= item
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+      }
+      const int b = lo;
+      const int nsplit = (prefix[b + 1] - prefix[b]) / p.Hkv;
+      const int local = item - prefix[b];
+      const int kvh = local / nsplit, split = local % nsplit;
+      const int L = clamp_len<P>(p, b);
+      const int start_tok = window_start(p, L);
+      const int sp = start_tok / P;
+      const int n = (L + P - 1) / P - sp;
+      const int p0 = sp + (int)((long long)n * split / nsplit);
+      const int p1 = sp + (int)((long long)n * (split + 1) / nsplit);
       if (lane == 0) {
         ItemDesc& d = items[slot];
-        d.item = cur; d.b = ci.b; d.kvh = ci.kvh; d.split = ci.split; d.nsplit = ci.nsplit;
-        d.p0 = ci.p0; d.p1 = ci.p1; d.start_tok = ci.start_tok; d.L = ci.L;
-        d.seq_base = (int)seq;
+        d.item = item; d.b = b; d.kvh = kvh; d.split = split; d.nsplit = nsplit;
+        d.p0 = p0; d.p1 = p1; d.start_tok = start_tok; d.L = L; d.seq_base = (int)seq;
         // the descriptor stores are released by this arrive; the phase also
         // waits for the 8 query rows
         mbar_arrive_expect_tx(ifull_bar(slot), kQBytes);
-        const uint16_t* qrow = p.q + ci.b * p.q_sb + (long long)(ci.kvh * kGqaGroup) * p.q_sh;
+        const uint16_t* qrow = p.q + b * p.q_sb + (long long)(kvh * kGqaGroup) * p.q_sh;
 #pragma unroll
         for (int h = 0; h < kGqaGroup; ++h)
           bulk_load(qbuf + slot * kQBytes + h * kGqaHeadDim * 2, qrow + h * p.q_sh,
                     kGqaHeadDim * 2, ifull_bar(slot));
       }
-      const int nx = __shfl_sync(0xffffffffu, nxt, 0);  // fetched one item ago
-      if (nx < total_items && lane == 0) nxt = atomicAdd(&p.sched[0], 1);
-      ItemInfo ni = {};
-      if (nx < total_items) ni = decode_item<P>(p, prefix, lens, nx);
-      for (int pb = ci.p0; pb < ci.p1; pb += 32) {
-        const int cnt = min(32, ci.p1 - pb);
-        const int blk = blk_pref;
-        if (pb + 32 < ci.p1)
-          blk_pref = load_bt_chunk(p, ci.b, pb + 32, ci.p1, lane);
-        else if (nx < total_items)
-          blk_pref = load_bt_chunk(p, ni.b, ni.p0, ni.p1, lane);
-        if (lane < cnt && (blk < 0 || blk >= p.num_blocks)) atomicOr(p.err, DEVERR_BAD_BLOCK);
+      const int32_t* bt_row = p.bt + (long long)b * p.bt_sb;
+      for (int pb = p0; pb < p1; pb += 32) {
+        const int cnt = min(32, p1 - pb);
+        int blk = 0;
+        if (lane < cnt) {
+          blk = __ldg(bt_row + pb + lane);
+          if (blk < 0 || blk >= p.num_blocks) atomicOr(p.err, DEVERR_BAD_BLOCK);
+        }
         for (int i = 0; i < cnt; ++i) {
           const int blk_i = __shfl_sync(0xffffffffu, blk, i);
 #pragma unroll
@@ -357,17 +321,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               const uint32_t dst = ring + stage * kStageBytes;
 #pragma unroll
               for (int c = 0; c < 4; ++c)
-                tma_load_4d(dst + c * kBoxBytes, &kv_map, full_bar(stage), 64 * c, 16 * sub,
-                            ci.kvh, blk_i);
+                tma_load_4d(dst + c * kBoxBytes, &kv_map, full_bar(stage), 64 * c, 16 * sub, kvh,
+                            blk_i);
             }
             ++seq;
           }
         }
       }
-      // an item without pages (an empty request) left the prefetch undone
-      if (ci.p1 <= ci.p0 && nx < total_items) blk_pref = load_bt_chunk(p, ni.b, ni.p0, ni.p1, lane);
-      cur = nx;
-      ci = ni;
     }
     if (lane == 0) {
       // every issued copy has landed before the CTA may exit (the consumers
