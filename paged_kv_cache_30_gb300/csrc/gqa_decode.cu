@@ -23,7 +23,9 @@
 //    full/empty mbarriers.  It runs ahead across item boundaries.
 //  * Consumer warp w takes tiles w, w+4, ... of the item.  It pulls the tile's
 //    K and V fragments into registers with ldmatrix (conflict-free thanks to
-//    the swizzle), frees the stage at once, then
+//    the swizzle), frees the stage at once (after a generic-to-async proxy
+//    fence: the next TMA write into the stage must not overtake these reads),
+//    then
 //      S[8 heads x 16 tok] = Q K^T          mma.m16n8k16, heads on the M side
 //                                             (rows 8..15 zero)
 //      online softmax, exp2 domain, running max in unscaled logits
@@ -372,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         qa[s][1] = *reinterpret_cast<const uint32_t*>(qs + (16 * s + 8 + 2 * t) * 2);
       }
     }
+    fence_proxy_async_smem();  // the Q slot is refilled by a bulk copy
     __syncwarp();
     if (lane == 0) mbar_arrive(iempty_bar(slot));
     if (d.item < 0) break;
@@ -401,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         ldsm_x4_trans(tile + (2 + (j >> 2)) * kBoxBytes + (unit << 4), vf[j][0], vf[j][1],
                       vf[j][2], vf[j][3]);
       }
+      fence_proxy_async_smem();  // the stage is refilled by TMA
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(stage));
 

@@ -138,6 +138,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {  // RNE, lo 
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA / bulk copy) accesses.  Needed before a buffer that
+// was read with ordinary loads (ldmatrix, ld.shared) is released to be
+// refilled by a bulk copy: the mbarrier arrive alone does not order the two
+// proxies.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
