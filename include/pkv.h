@@ -142,6 +142,42 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
                                   const pkv_tensor* lse, void* stream);
 
 /*
+ * pkv_paged_decode_attn_noalloc -- pkv_paged_decode_attn on scratch memory the
+ * library never allocates.  The pages have no counterpart: this entry point
+ * exists for callers that cannot let a library call cudaMalloc, e.g. a serving
+ * engine that reserves all of HBM for its own KV-cache pool and treats any
+ * other device allocation as an out-of-memory risk, a framework whose memory
+ * manager must own every device buffer, or code that runs while a stream
+ * capture forbids allocation.
+ *
+ * Arguments, layouts, results and error codes are those of
+ * pkv_paged_decode_attn.  The split partials, arrival counters and work-queue
+ * words live in one file-scope __device__ array of about 8.2 MiB that every
+ * GPU loading the library holds until the process exits.  Limits: batch x kv
+ * heads <= 4096 and batch x kv heads x splits <= 2048 (the split cap is chosen
+ * to fit when num_kv_splits is 0); larger calls return PKV_ERR_WORKSPACE and
+ * launch nothing.  The call allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine, and it never touches the workspace of
+ * pkv_init.  Each call clears the array's counters with cudaMemsetAsync on
+ * `stream` before its launch.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress); make that first call before any stream
+ *     capture.
+ *   - Every call shares the one array: calls whose kernels may overlap on the
+ *     GPU (different streams without ordering, different threads) race and
+ *     give wrong results.  Order them on one stream.
+ *   - Device-side input errors (bad block-table entries) are clamped or
+ *     zero-filled as on the allocating path but are not reported:
+ *     pkv_check_errors does not see this path.
+ */
+PKV_API int pkv_paged_decode_attn_noalloc(const pkv_tensor* q, const pkv_tensor* kv_cache,
+                                          const pkv_tensor* block_table,
+                                          const pkv_tensor* seq_lens, const pkv_tensor* sinks,
+                                          int window, float scale, int page_size,
+                                          int num_kv_splits, const pkv_tensor* out,
+                                          const pkv_tensor* lse, void* stream);
+
+/*
  * pkv_mla_verify_attn -- causal MLA verify over a per-request block table.
  * Source: "vllm.v1.attention.ops.triton_decode_attention",
  * decode_attention_fwd_verify (parameters).

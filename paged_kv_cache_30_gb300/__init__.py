@@ -10,6 +10,7 @@ Names follow the C ABI without its ``pkv_`` prefix:
 
     paged_decode_attn(q, kv_cache, block_table, seq_lens, sinks, window, scale,
                       page_size, num_kv_splits, out, lse=None, stream=None)
+    paged_decode_attn_noalloc(...)   same arguments; allocates nothing
     mla_verify_attn(q, latent_cache, block_table, seq_lens, real_seq_lens, qlen,
                     scale, page_size, k_scale, out, lse, num_kv_splits=0,
                     stream=None)
@@ -25,6 +26,7 @@ import threading
 
 __all__ = [
     "PkvError", "load_library", "library_path", "init", "paged_decode_attn",
+    "paged_decode_attn_noalloc",
     "mla_verify_attn", "num_kv_splits", "check_errors", "check_counters", "shutdown",
     "version", "last_error",
 ]
@@ -76,12 +78,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         i32, f32, vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
         lib.pkv_init.argtypes = [i32, ctypes.c_size_t]
         lib.pkv_paged_decode_attn.argtypes = [T, T, T, T, T, i32, f32, i32, i32, T, T, vp]
+        lib.pkv_paged_decode_attn_noalloc.argtypes = [T, T, T, T, T, i32, f32, i32, i32, T, T, vp]
         lib.pkv_mla_verify_attn.argtypes = [T, T, T, T, T, i32, f32, i32, T, T, T, i32, vp]
         lib.pkv_num_kv_splits.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_double, i32, i32]
         lib.pkv_check_errors.argtypes = [i32, ctypes.POINTER(ctypes.c_int32)]
         lib.pkv_check_counters.argtypes = [i32, ctypes.POINTER(ctypes.c_int64)]
         lib.pkv_last_error.restype = ctypes.c_char_p
-        for name in ("pkv_init", "pkv_paged_decode_attn", "pkv_mla_verify_attn",
+        for name in ("pkv_init", "pkv_paged_decode_attn", "pkv_paged_decode_attn_noalloc",
+                     "pkv_mla_verify_attn",
                      "pkv_num_kv_splits", "pkv_check_errors", "pkv_check_counters",
                      "pkv_shutdown", "pkv_version"):
             getattr(lib, name).restype = i32
@@ -145,6 +149,21 @@ def paged_decode_attn(q, kv_cache, block_table, seq_lens, sinks, window, scale, 
     stream of q's device) and returns ``out``."""
     lib = load_library()
     _check(lib.pkv_paged_decode_attn(
+        _desc(q), _desc(kv_cache), _desc(block_table), _desc(seq_lens), _desc(sinks),
+        int(window or 0), float(scale), int(page_size), int(num_kv_splits), _desc(out),
+        _desc(lse), _stream(stream, q)))
+    return out
+
+
+def paged_decode_attn_noalloc(q, kv_cache, block_table, seq_lens, sinks, window, scale,
+                              page_size, num_kv_splits, out, lse=None, stream=None):
+    """GQA paged decode attention that allocates nothing (C:
+    pkv_paged_decode_attn_noalloc): for callers that cannot let a library
+    allocate device memory.  Its scratch is a fixed array inside the library
+    (batch x kv heads <= 4096, batch x kv heads x splits <= 2048); calls must
+    not overlap on the GPU."""
+    lib = load_library()
+    _check(lib.pkv_paged_decode_attn_noalloc(
         _desc(q), _desc(kv_cache), _desc(block_table), _desc(seq_lens), _desc(sinks),
         int(window or 0), float(scale), int(page_size), int(num_kv_splits), _desc(out),
         _desc(lse), _stream(stream, q)))

@@ -469,3 +469,118 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Shared with entry points implemented in other translation units.
+namespace pkv {
+
+int abi_fail(int code, const char* message) { return fail(code, "%s", message); }
+
+int abi_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+
+int prepare_gqa_call(const pkv_tensor* q, const pkv_tensor* kv_cache,
+                     const pkv_tensor* block_table, const pkv_tensor* seq_lens,
+                     const pkv_tensor* sinks, int window, float scale, int page_size,
+                     int num_kv_splits, const pkv_tensor* out, const pkv_tensor* lse,
+                     GqaCall* call) {
+  int rc;
+  if ((rc = check_tensor(q, "q", PKV_DTYPE_BF16, 3))) return rc;
+  if ((rc = check_tensor(kv_cache, "kv_cache", PKV_DTYPE_BF16, 4))) return rc;
+  if ((rc = check_tensor(block_table, "block_table", PKV_DTYPE_I32, 2))) return rc;
+  if ((rc = check_tensor(seq_lens, "seq_lens", PKV_DTYPE_I32, 1))) return rc;
+  if ((rc = check_tensor(out, "out", PKV_DTYPE_BF16, 3))) return rc;
+  if (sinks && (rc = check_tensor(sinks, "sinks", PKV_DTYPE_F32, 1))) return rc;
+  if (lse && (rc = check_tensor(lse, "lse", PKV_DTYPE_F32, 2))) return rc;
+  const int64_t B = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  const int64_t nb = kv_cache->shape[0], Hkv = kv_cache->shape[1];
+  if (D != kGqaHeadDim)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %lld (only 128 is built)", (long long)D);
+  if (kv_cache->shape[3] != 2 * D)
+    return fail(PKV_ERR_INVALID_ARG, "kv_cache last dim %lld, expected [K | V] = 256",
+                (long long)kv_cache->shape[3]);
+  if (Hkv <= 0 || Hq != kGqaGroup * Hkv)
+    return fail(PKV_ERR_UNSUPPORTED, "num_q_heads %lld must be 8 x num_kv_heads %lld",
+                (long long)Hq, (long long)Hkv);
+  if (page_size != 16 && page_size != 32)
+    return fail(PKV_ERR_UNSUPPORTED, "page_size %d (16 and 32 are built)", page_size);
+  if (kv_cache->shape[2] != page_size)
+    return fail(PKV_ERR_INVALID_ARG, "kv_cache.shape[2] %lld != page_size %d",
+                (long long)kv_cache->shape[2], page_size);
+  if (nb < 1 || nb >= (int64_t(1) << 31))
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks %lld", (long long)nb);
+  if (block_table->shape[0] != B || seq_lens->shape[0] != B)
+    return fail(PKV_ERR_INVALID_ARG, "block_table / seq_lens batch mismatch");
+  if (out->shape[0] != B || out->shape[1] != Hq || out->shape[2] != D)
+    return fail(PKV_ERR_INVALID_ARG, "out shape mismatch");
+  if (sinks && sinks->shape[0] != Hq) return fail(PKV_ERR_INVALID_ARG, "sinks must be [Hq]");
+  if (sinks && sinks->shape[0] > 1 && sinks->stride[0] != 1)
+    return fail(PKV_ERR_INVALID_ARG, "sinks must be contiguous");
+  if (lse && (lse->shape[0] != B || lse->shape[1] != Hq))
+    return fail(PKV_ERR_INVALID_ARG, "lse must be [B, Hq]");
+  if (block_table->shape[1] < 1 || block_table->shape[1] > (int64_t(1) << 30))
+    return fail(PKV_ERR_INVALID_ARG, "block_table width %lld", (long long)block_table->shape[1]);
+  if (block_table->stride[1] != 1 && block_table->shape[1] > 1)
+    return fail(PKV_ERR_INVALID_ARG, "block_table rows must be contiguous");
+  if (seq_lens->stride[0] != 1 && B > 1)
+    return fail(PKV_ERR_INVALID_ARG, "seq_lens must be contiguous");
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (num_kv_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_splits < 0");
+  if (B > kGqaMaxBatch)
+    return fail(PKV_ERR_UNSUPPORTED, "batch %lld > %d", (long long)B, kGqaMaxBatch);
+  if (q->stride[2] != 1 || out->stride[2] != 1 || kv_cache->stride[3] != 1 ||
+      kv_cache->stride[2] != 2 * D)
+    return fail(PKV_ERR_INVALID_ARG, "q/out last dim and kv_cache rows must be contiguous");
+  if (q->stride[0] % 8 || q->stride[1] % 8 || out->stride[0] % 8 || out->stride[1] % 8 ||
+      kv_cache->stride[0] % 8 || kv_cache->stride[1] % 8)
+    return fail(PKV_ERR_ALIGNMENT, "strides of q, out and kv_cache must be multiples of 8");
+  if (!aligned16(q->data) || !aligned16(out->data) || !aligned16(kv_cache->data))
+    return fail(PKV_ERR_ALIGNMENT, "q, out and kv_cache must be 16-byte aligned");
+
+  std::memset(call, 0, sizeof *call);
+  call->pairs = B * Hkv;
+  call->cap_req = num_kv_splits;
+  call->page_size = page_size;
+  if (B == 0) return PKV_OK;
+
+  EncodeTiledFn encode = nullptr;
+  if ((rc = get_encoder(&encode))) return rc;
+  const cuuint64_t gdim[4] = {cuuint64_t(2 * D), cuuint64_t(page_size), cuuint64_t(Hkv),
+                              cuuint64_t(nb)};
+  const cuuint64_t gstride[3] = {cuuint64_t(kv_cache->stride[2]) * 2,
+                                 cuuint64_t(kv_cache->stride[1]) * 2,
+                                 cuuint64_t(kv_cache->stride[0]) * 2};
+  const cuuint32_t box[4] = {64, 16, 1, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  const CUresult cr = encode(&call->map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, kv_cache->data,
+                             gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS)
+    return fail(PKV_ERR_INVALID_ARG, "cuTensorMapEncodeTiled rejected the kv_cache layout (%d)",
+                (int)cr);
+  GqaParams& p = call->p;
+  p.q = static_cast<const uint16_t*>(q->data);
+  p.q_sb = q->stride[0];
+  p.q_sh = q->stride[1];
+  p.bt = static_cast<const int32_t*>(block_table->data);
+  p.bt_sb = block_table->stride[0];
+  p.max_blocks = int(block_table->shape[1]);
+  p.num_blocks = int(nb);
+  p.seq_lens = static_cast<const int32_t*>(seq_lens->data);
+  p.sinks = sinks ? static_cast<const float*>(sinks->data) : nullptr;
+  p.out = static_cast<uint16_t*>(out->data);
+  p.o_sb = out->stride[0];
+  p.o_sh = out->stride[1];
+  p.lse = lse ? static_cast<float*>(lse->data) : nullptr;
+  p.lse_sb = lse ? lse->stride[0] : 0;
+  p.lse_sh = lse ? lse->stride[1] : 0;
+  p.B = int(B);
+  p.Hkv = int(Hkv);
+  p.window = window;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale = scale;
+  p.min_pages = 256 / page_size;
+  return PKV_OK;
+}
+
+}  // namespace pkv

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+struct pkv_tensor;  // include/pkv.h
+
 namespace pkv {
 
 // Device-side error bits, OR-ed into the workspace error word and read back by
@@ -69,6 +71,25 @@ struct GqaParams {
 cudaError_t launch_gqa_decode(const GqaParams& p, const CUtensorMap& kv_map, int page_size,
                               int grid, cudaStream_t stream);
 int gqa_ctas_per_sm();
+
+// A validated GQA decode call: kernel parameters (without workspace pointers)
+// and the KV-cache tensor map.
+struct GqaCall {
+  GqaParams p;
+  alignas(64) CUtensorMap map;
+  int64_t pairs;   // B * Hkv
+  int cap_req;     // num_kv_splits as given (0 = library's choice)
+  int page_size;
+};
+
+// Defined in api.cpp, for entry points implemented in other files.
+int prepare_gqa_call(const ::pkv_tensor* q, const ::pkv_tensor* kv_cache,
+                     const ::pkv_tensor* block_table, const ::pkv_tensor* seq_lens,
+                     const ::pkv_tensor* sinks, int window, float scale, int page_size,
+                     int num_kv_splits, const ::pkv_tensor* out, const ::pkv_tensor* lse,
+                     GqaCall* call);
+int abi_fail(int code, const char* message);
+int abi_cuda_fail(cudaError_t e, const char* what);
 
 // The counter region of the workspace holds 2^20 ints: the first half for
 // (request, kv head) counters, the second half for split-group counters.
