@@ -461,11 +461,152 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
                                 const pkv_tensor* block_table, const pkv_tensor* seq_lens,
                                 const pkv_tensor* real_seq_lens, int qlen, float scale,
                                 int page_size, const pkv_tensor* k_scale, const pkv_tensor* out,
-                                const pkv_tensor* lse, int num_kv_splits, void* stream) {
-  (void)q; (void)latent_cache; (void)block_table; (void)seq_lens; (void)real_seq_lens;
-  (void)qlen; (void)scale; (void)page_size; (void)k_scale; (void)out; (void)lse;
-  (void)num_kv_splits; (void)stream;
-  return fail(PKV_ERR_UNSUPPORTED, "the MLA verify kernel is not built yet");
+                                const pkv_tensor* lse, int num_kv_splits, void* stream_ptr) {
+  int rc;
+  if ((rc = check_tensor(q, "q", PKV_DTYPE_BF16, 3))) return rc;
+  if (!latent_cache) return fail(PKV_ERR_INVALID_ARG, "latent_cache is NULL");
+  const bool fp8 = latent_cache->dtype == PKV_DTYPE_FP8_E4M3;
+  if ((rc = check_tensor(latent_cache, "latent_cache", fp8 ? PKV_DTYPE_FP8_E4M3 : PKV_DTYPE_BF16,
+                         latent_cache->ndim == 3 ? 3 : 4)))
+    return rc;
+  if ((rc = check_tensor(block_table, "block_table", PKV_DTYPE_I32, 2))) return rc;
+  if ((rc = check_tensor(seq_lens, "seq_lens", PKV_DTYPE_I32, 1))) return rc;
+  if (real_seq_lens && (rc = check_tensor(real_seq_lens, "real_seq_lens", PKV_DTYPE_I32, 1)))
+    return rc;
+  if ((rc = check_tensor(out, "out", PKV_DTYPE_BF16, 3))) return rc;
+  if ((rc = check_tensor(lse, "lse", PKV_DTYPE_F32, 2))) return rc;
+  if (k_scale) {
+    if (!k_scale->data || k_scale->dtype != PKV_DTYPE_F32 ||
+        !(k_scale->ndim == 0 || (k_scale->ndim == 1 && k_scale->shape[0] == 1)))
+      return fail(PKV_ERR_INVALID_ARG, "k_scale must be an fp32 scalar on the device");
+  }
+  if (qlen < 1) return fail(PKV_ERR_INVALID_ARG, "qlen %d < 1", qlen);
+  const int64_t R = q->shape[0], H = q->shape[1], Lk = q->shape[2];
+  if (H != pkv::kMlaHeads) return fail(PKV_ERR_UNSUPPORTED, "%lld heads (128 are built)", (long long)H);
+  if (Lk != pkv::kMlaLk) return fail(PKV_ERR_UNSUPPORTED, "Lk %lld (576 is built)", (long long)Lk);
+  if (R % qlen) return fail(PKV_ERR_INVALID_ARG, "q rows %lld not a multiple of qlen %d", (long long)R, qlen);
+  const int64_t B = R / qlen;
+  if (page_size != 16 && page_size != 32)
+    return fail(PKV_ERR_UNSUPPORTED, "page_size %d (16 and 32 are built)", page_size);
+  // latent cache: [num_pages, P, 1, 576] or [num_pages * P, 1, 576]
+  int64_t num_pages, s_page, s_tok;
+  if (latent_cache->ndim == 4) {
+    if (latent_cache->shape[1] != page_size || latent_cache->shape[2] != 1 ||
+        latent_cache->shape[3] != Lk)
+      return fail(PKV_ERR_INVALID_ARG, "latent_cache must be [num_pages, %d, 1, 576]", page_size);
+    num_pages = latent_cache->shape[0];
+    s_page = latent_cache->stride[0];
+    s_tok = latent_cache->stride[1];
+    if (latent_cache->stride[3] != 1)
+      return fail(PKV_ERR_INVALID_ARG, "latent rows must be contiguous");
+  } else {
+    if (latent_cache->shape[1] != 1 || latent_cache->shape[2] != Lk ||
+        latent_cache->shape[0] % page_size)
+      return fail(PKV_ERR_INVALID_ARG, "latent_cache must be [num_pages * P, 1, 576]");
+    num_pages = latent_cache->shape[0] / page_size;
+    s_tok = latent_cache->stride[0];
+    s_page = s_tok * page_size;
+    if (latent_cache->stride[2] != 1)
+      return fail(PKV_ERR_INVALID_ARG, "latent rows must be contiguous");
+  }
+  const int esz = fp8 ? 1 : 2;
+  if (num_pages < 1 || num_pages >= (int64_t(1) << 31))
+    return fail(PKV_ERR_INVALID_ARG, "num_pages %lld", (long long)num_pages);
+  if ((s_tok * esz) % 16 || (s_page * esz) % 16 || !aligned16(latent_cache->data))
+    return fail(PKV_ERR_ALIGNMENT, "latent cache rows and pages must be 16-byte aligned");
+  if (block_table->shape[0] != B || seq_lens->shape[0] != B ||
+      (real_seq_lens && real_seq_lens->shape[0] != B))
+    return fail(PKV_ERR_INVALID_ARG, "block_table / seq_lens / real_seq_lens batch mismatch");
+  if (block_table->shape[1] < 1 || (block_table->stride[1] != 1 && block_table->shape[1] > 1))
+    return fail(PKV_ERR_INVALID_ARG, "block_table rows must be non-empty and contiguous");
+  if ((seq_lens->stride[0] != 1 && B > 1) ||
+      (real_seq_lens && real_seq_lens->stride[0] != 1 && B > 1))
+    return fail(PKV_ERR_INVALID_ARG, "seq_lens must be contiguous");
+  if (out->shape[0] != R || out->shape[1] != H || out->shape[2] != pkv::kMlaLv)
+    return fail(PKV_ERR_INVALID_ARG, "out must be [B*qlen, 128, 512]");
+  if (lse->shape[0] != R || lse->shape[1] != H)
+    return fail(PKV_ERR_INVALID_ARG, "lse must be [B*qlen, 128]");
+  if (q->stride[2] != 1 || out->stride[2] != 1)
+    return fail(PKV_ERR_INVALID_ARG, "q and out last dims must be contiguous");
+  if (q->stride[0] % 8 || q->stride[1] % 8 || out->stride[0] % 8 || out->stride[1] % 8 ||
+      !aligned16(q->data) || !aligned16(out->data))
+    return fail(PKV_ERR_ALIGNMENT, "q and out must be 16-byte aligned with strides % 8 == 0");
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (num_kv_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_splits < 0");
+  if (fp8) return fail(PKV_ERR_UNSUPPORTED, "the FP8 latent cache path is not built yet");
+  if (B == 0) return PKV_OK;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int dev = 0;
+  DeviceState* st = nullptr;
+  bool capturing = false;
+  if ((rc = workspace_for(stream, &dev, &st, &capturing))) return rc;
+  const pkv::Workspace& ws = st->ws;
+  // splits: at most 16 per (request, token, half); the device uses fewer for
+  // short requests (at least 1024 keys per split)
+  int64_t cap = num_kv_splits == 0 ? 16 : std::min<int64_t>(num_kv_splits, 16);
+  const int64_t max_slots = int64_t(ws.partial_bytes) / (pkv::kMlaPartialFloats * 4);
+  const int64_t units = B * qlen * 2;
+  if (units > pkv::kTopCounters)
+    return fail(PKV_ERR_WORKSPACE, "%lld (row, half) units exceed the counters", (long long)units);
+  if (num_kv_splits == 0) cap = std::max<int64_t>(1, std::min<int64_t>(cap, max_slots / units));
+  if (units * cap > max_slots || units * cap >= (int64_t(1) << 31))
+    return fail(PKV_ERR_WORKSPACE, "workspace holds %lld MLA partials, %lld needed",
+                (long long)max_slots, (long long)(units * cap));
+
+  EncodeTiledFn encode = nullptr;
+  if ((rc = get_encoder(&encode))) return rc;
+  alignas(64) CUtensorMap q_map, kv_map;
+  {
+    const cuuint64_t gdim[3] = {cuuint64_t(Lk), cuuint64_t(H), cuuint64_t(R)};
+    const cuuint64_t gstr[2] = {cuuint64_t(q->stride[1]) * 2, cuuint64_t(q->stride[0]) * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult cr = encode(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q->data, gdim, gstr, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return fail(PKV_ERR_INVALID_ARG, "q tensor map rejected (%d)", (int)cr);
+  }
+  {
+    const cuuint64_t gdim[3] = {cuuint64_t(Lk), cuuint64_t(page_size), cuuint64_t(num_pages)};
+    const cuuint64_t gstr[2] = {cuuint64_t(s_tok) * esz, cuuint64_t(s_page) * esz};
+    const cuuint32_t box[3] = {64, 16, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult cr = encode(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, latent_cache->data, gdim,
+                         gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS)
+      return fail(PKV_ERR_INVALID_ARG, "latent cache tensor map rejected (%d)", (int)cr);
+  }
+  pkv::MlaParams p;
+  std::memset(&p, 0, sizeof p);
+  p.bt = static_cast<const int32_t*>(block_table->data);
+  p.bt_sb = block_table->stride[0];
+  p.max_blocks = int(std::min<int64_t>(block_table->shape[1], int64_t(1) << 30));
+  p.num_pages = int(num_pages);
+  p.seq_lens = static_cast<const int32_t*>(seq_lens->data);
+  p.real_seq_lens = real_seq_lens ? static_cast<const int32_t*>(real_seq_lens->data) : nullptr;
+  p.k_scale = k_scale ? static_cast<const float*>(k_scale->data) : nullptr;
+  p.out = static_cast<uint16_t*>(out->data);
+  p.o_sr = out->stride[0];
+  p.o_sh = out->stride[1];
+  p.lse = static_cast<float*>(lse->data);
+  p.lse_sr = lse->stride[0];
+  p.lse_sh = lse->stride[1];
+  p.B = int(B);
+  p.qlen = qlen;
+  p.cap = int(cap);
+  p.page_size = page_size;
+  p.scale = scale;
+  p.partials = ws.partials;
+  p.max_slots = max_slots;
+  p.counters = ws.counters;
+  p.err = ws.err;
+  if ((rc = order_streams(st, stream, capturing))) return rc;
+  const cudaError_t e =
+      pkv::launch_mla_verify(p, q_map, kv_map, fp8, int(units * cap), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "mla verify launch");
+  return PKV_OK;
 }
 
 }  // extern "C"

@@ -1,0 +1,446 @@
+// mla_verify.cu -- causal MLA verify over a paged latent cache, on tcgen05.
+//
+// Computes, for verify token t of request b (row r = b * qlen + t) and each
+// of the 128 query heads h,
+//   out[r, h, :] = sum_{j < lim} softmax_j(scale * q[r, h, :] . K_j) K_j[:512]
+//   lse[r, h]    = log sum_{j < lim} exp(scale * q . K_j)   (-inf, out 0 if lim == 0)
+// with lim = max(min(L - qlen + 1 + t, L_real), 0) and K_j the 576-wide latent
+// row of key j gathered through block_table; V is the first 512 dims of K
+// ("vllm.v1.attention.ops.triton_decode_attention", decode_attention_fwd_verify:
+// parameters).  An FP8 e4m3 cache is dequantised by the scalar k_scale.
+//
+// One CTA per (request, split, verify token, half of the 512 output dims);
+// inactive splits return at once.  Tensor memory (512 columns) holds the
+// CTA's output half O[128 x 256] (fp32) and two score buffers S[128 x 32].
+//   warp 0      TMA: the token's 128 x 576 query tile once, then 32-key tiles
+//               of the latent cache (9 boxes of 64 dims per 16-token page
+//               piece, 128-byte swizzle) into a 2-stage ring.
+//   warp 1      TMEM allocation; one thread issues the MMAs:
+//               S = Q K^T  (M 128 heads, N 32 keys, K 576: 36 x K16, both
+//               operands K-major) and O += P V (M 128, N 256, K 32; P
+//               K-major with 64-byte swizzle, V = the same smem tile read
+//               MN-major).
+//   warps 4..7  softmax, one thread per head: S from TMEM, mask j >= lim,
+//               exp2-domain online softmax with a lazily updated max (O in
+//               TMEM is rescaled only when the max grows by more than 2^8),
+//               P rounded to bf16 into shared memory; epilogue.
+// The two halves both compute S (576-wide Q K^T) and each does half of P V.
+// Splits of a request publish fp32 (O half, m, l) partials; the last CTA of a
+// (request, token, half) merges them and resets its arrival counter.
+#include "pkv_internal.h"
+#include "ptx.cuh"
+#include "tcgen05.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kSoftmaxWarp0 = 4;
+constexpr int kStages = 2;
+constexpr int kChunks = kMlaLk / 64;            // 9 64-dim chunks of a latent row
+constexpr int kQChunkBytes = kMlaHeads * 128;   // 16 KB: 128 rows x 64 dims
+constexpr int kKChunkBytes = kMlaTile * 128;    // 4 KB: 32 keys x 64 dims
+constexpr int kQBytes = kChunks * kQChunkBytes;     // 147456
+constexpr int kStageBytes = kChunks * kKChunkBytes; // 36864
+constexpr int kPBytes = kMlaHeads * kMlaTile * 2;   // 8192 (64-byte rows)
+constexpr int kOffStages = kQBytes;
+constexpr int kOffP = kOffStages + kStages * kStageBytes;
+constexpr int kOffBars = kOffP + kPBytes;
+constexpr int kSmemBytes = kOffBars + 128 + 1024;
+static_assert(kOffStages % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1024 B alignment");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 0;     // columns [0, 256): O half
+constexpr uint32_t kTmemS = 256;   // columns [256, 320): two S buffers of 32
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+
+// barrier indices
+enum { kQFull = 0, kKvFull = 1, kKvEmpty = 3, kSFull = 5, kSFree = 7, kPFull = 9, kPvDone = 10,
+       kNumBars = 11 };
+
+struct Unit {
+  int b, split, t, half, nsplit;
+  int L, lim;
+  int tile0, ntiles;  // tiles [tile0, tile0 + ntiles) of this CTA
+};
+
+__device__ __forceinline__ Unit decode_unit(const MlaParams& p) {
+  Unit u;
+  int x = blockIdx.x;
+  u.half = x & 1;
+  x >>= 1;
+  u.t = x % p.qlen;
+  x /= p.qlen;
+  u.split = x % p.cap;
+  u.b = x / p.cap;
+  int L = __ldg(p.seq_lens + u.b);
+  if (L < 0) L = 0;
+  if ((long long)L > (long long)p.max_blocks * p.page_size) L = p.max_blocks * p.page_size;
+  int Lr = p.real_seq_lens ? __ldg(p.real_seq_lens + u.b) : L;
+  int lim = L - p.qlen + 1 + u.t;
+  if (Lr < lim) lim = Lr;
+  if (lim < 0) lim = 0;
+  u.L = L;
+  u.lim = lim;
+  const int req_tiles = (L + kMlaTile - 1) / kMlaTile;
+  int ns = (req_tiles + kMlaMinTiles - 1) / kMlaMinTiles;
+  ns = ns < 1 ? 1 : (ns > p.cap ? p.cap : ns);
+  u.nsplit = ns;
+  const int a = (int)((long long)req_tiles * u.split / ns);
+  const int e = (int)((long long)req_tiles * (u.split + 1) / ns);
+  const int lim_tiles = (lim + kMlaTile - 1) / kMlaTile;
+  u.tile0 = a;
+  u.ntiles = max(0, min(e, lim_tiles) - a);
+  return u;
+}
+
+__device__ __forceinline__ int counter_index(const MlaParams& p, const Unit& u) {
+  return (u.b * p.qlen + u.t) * 2 + u.half;
+}
+
+__device__ __forceinline__ long long slot_of(const MlaParams& p, const Unit& u, int split) {
+  return ((long long)(u.b * p.cap + split) * p.qlen + u.t) * 2 + u.half;
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_verify_kernel(const __grid_constant__ MlaParams p, const __grid_constant__ CUtensorMap q_map,
+                      const __grid_constant__ CUtensorMap kv_map) {
+  const Unit u = decode_unit(p);
+  if (u.split >= u.nsplit) return;  // this request needs fewer splits
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  const uint32_t sQ = base_u32, sK = base_u32 + kOffStages, sP = base_u32 + kOffP;
+  const uint32_t bars = base_u32 + kOffBars;
+  auto bar = [&](int i) { return bars + 8u * i; };
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + kOffBars + 8 * kNumBars);
+  int* flag = reinterpret_cast<int*>(base + kOffBars + 8 * kNumBars + 16);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(bar(kQFull), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kKvFull + s), 1);
+      mbar_init(bar(kKvEmpty + s), 1);
+      mbar_init(bar(kSFull + s), 1);
+      mbar_init(bar(kSFree + s), 128);
+    }
+    mbar_init(bar(kPFull), 1);
+    mbar_init(bar(kPvDone), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  float scale_eff = p.scale;
+  if (kFp8 && p.k_scale) scale_eff *= __ldg(p.k_scale);
+  const float c2 = scale_eff * kLog2e;
+  const int n = u.ntiles;
+
+  if (warp == 0) {
+    // ============================ TMA producer ============================
+    if (n > 0) {
+      const int qrow = u.b * p.qlen + u.t;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(kQFull), kQBytes);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_3d(sQ + c * kQChunkBytes, &q_map, bar(kQFull), 64 * c, 0, qrow);
+      }
+      const int32_t* bt_row = p.bt + (long long)u.b * p.bt_sb;
+      for (int g = 0; g < n; g += 16) {
+        // lane l holds the block id of 16-key piece l of tiles [g, g + 16)
+        const int piece_tok = (u.tile0 + g) * kMlaTile + 16 * lane;
+        int blk = p.num_pages;  // out of range: TMA fills zeros
+        int off = 0;
+        if (piece_tok < u.L && lane < 2 * (n - g)) {
+          blk = __ldg(bt_row + piece_tok / p.page_size);
+          off = piece_tok % p.page_size;
+          if (blk < 0 || blk >= p.num_pages) atomicOr(p.err, DEVERR_BAD_BLOCK);
+        }
+        for (int i = g; i < min(n, g + 16); ++i) {
+          const int b0 = __shfl_sync(0xffffffffu, blk, 2 * (i - g));
+          const int o0 = __shfl_sync(0xffffffffu, off, 2 * (i - g));
+          const int b1 = __shfl_sync(0xffffffffu, blk, 2 * (i - g) + 1);
+          const int o1 = __shfl_sync(0xffffffffu, off, 2 * (i - g) + 1);
+          if (lane == 0) {
+            const int st = i % kStages;
+            mbar_wait(bar(kKvEmpty + st), ((i / kStages) & 1) ^ 1u, p.err);
+            mbar_arrive_expect_tx(bar(kKvFull + st), kStageBytes);
+            const uint32_t dst = sK + st * kStageBytes;
+            for (int c = 0; c < kChunks; ++c) {
+              tma_load_3d(dst + c * kKChunkBytes, &kv_map, bar(kKvFull + st), 64 * c, o0, b0);
+              tma_load_3d(dst + c * kKChunkBytes + 2048, &kv_map, bar(kKvFull + st), 64 * c, o1,
+                          b1);
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ============================= MMA issuer =============================
+    if (n > 0 && lane == 0) {
+      const uint32_t id_s = tc::idesc_bf16_f32(128, kMlaTile, false, false);
+      const uint32_t id_pv = tc::idesc_bf16_f32(128, kMlaHalf, false, true);
+      mbar_wait(bar(kQFull), 0, p.err);
+      auto do_pv = [&](int j) {
+        mbar_wait(bar(kPFull), j & 1, p.err);
+        tc::fence_after_sync();
+        const uint32_t v0 = sK + (j % kStages) * kStageBytes + (4 * u.half) * kKChunkBytes;
+#pragma unroll
+        for (int ks = 0; ks < kMlaTile / 16; ++ks)
+          tc::mma_bf16(tmem + kTmemO, tc::smem_desc(sP + ks * 32, 16, 512, tc::kSwizzle64),
+                       tc::smem_desc(v0 + ks * 2048, kKChunkBytes, 1024, tc::kSwizzle128), id_pv,
+                       j > 0 || ks > 0);
+        tc::commit(bar(kPvDone));
+        tc::commit(bar(kKvEmpty + j % kStages));
+      };
+      for (int i = 0; i < n; ++i) {
+        const int st = i % kStages, sb = i & 1;
+        mbar_wait(bar(kKvFull + st), (i / kStages) & 1, p.err);
+        mbar_wait(bar(kSFree + sb), ((i >> 1) & 1) ^ 1u, p.err);
+        tc::fence_after_sync();
+        const uint32_t kst = sK + st * kStageBytes;
+        for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_bf16(tmem + kTmemS + sb * kMlaTile,
+                         tc::smem_desc(sQ + c * kQChunkBytes + ks * 32, 16, 1024, tc::kSwizzle128),
+                         tc::smem_desc(kst + c * kKChunkBytes + ks * 32, 16, 1024, tc::kSwizzle128),
+                         id_s, (c | ks) != 0);
+        }
+        tc::commit(bar(kSFull + sb));
+        if (i > 0) do_pv(i - 1);
+      }
+      do_pv(n - 1);
+    }
+  } else if (warp >= kSoftmaxWarp0) {
+    // ================= softmax (one thread per head) + epilogue ============
+    const int row = tid - kSoftmaxWarp0 * 32;           // head 0..127
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    uint8_t* p_row = base + kOffP + (row / 8) * 512 + (row % 8) * 64;
+    const int pswz = (row % 8) >> 1;
+    for (int i = 0; i < n; ++i) {
+      const int sb = i & 1;
+      mbar_wait(bar(kSFull + sb), (i >> 1) & 1, p.err);
+      __syncwarp();  // tcgen05.ld is warp-collective
+      tc::fence_after_sync();
+      uint32_t xr[32];
+      tc::ld_32x32b_x32(tmem + lane_base + kTmemS + sb * kMlaTile, xr);
+      tc::wait_ld();
+      tc::fence_before_sync();
+      mbar_arrive(bar(kSFree + sb));
+      const int tok0 = (u.tile0 + i) * kMlaTile;
+      const int nvalid = min(kMlaTile, u.lim - tok0);
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kMlaTile; ++c)
+        if (c < nvalid) mt = fmaxf(mt, __uint_as_float(xr[c]));
+      // Lazy max: a row moves its reference max only when the tile's max
+      // exceeds it by more than 2^8 (or on its first key).  The TMEM accesses
+      // of the rescale are warp-collective, so the whole warp rescales when
+      // any of its rows needs to; each row uses its own factor (1 if unchanged).
+      bool waited = false;
+      const bool need =
+          mt > -INFINITY && (m_used == -INFINITY || (mt - m_used) * c2 > kRescaleLog2);
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mt : m_used;
+        const float alpha =
+            (m_used == -INFINITY) ? 0.f : (need ? ex2((m_used - m_new) * c2) : 1.f);
+        if (i > 0) {
+          // every P V so far must be done before O is rescaled in place
+          mbar_wait(bar(kPvDone), (i - 1) & 1, p.err);
+          waited = true;
+          __syncwarp();
+          tc::fence_after_sync();
+          for (int j = 0; j < kMlaHalf / 32; ++j) {
+            uint32_t o[32];
+            const uint32_t ta = tmem + lane_base + kTmemO + 32 * j;
+            tc::ld_32x32b_x32(ta, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tc::st_32x32b_x32(ta, o);
+          }
+          tc::wait_st();
+        }
+        l *= alpha;
+        m_used = m_new;
+      }
+      const float msc = (m_used == -INFINITY) ? 0.f : m_used * c2;
+      uint32_t pk[16];
+      float lt = 0.f;
+#pragma unroll
+      for (int c = 0; c < kMlaTile; c += 2) {
+        const float e0 = (c < nvalid) ? ex2(__fmaf_rn(__uint_as_float(xr[c]), c2, -msc)) : 0.f;
+        const float e1 =
+            (c + 1 < nvalid) ? ex2(__fmaf_rn(__uint_as_float(xr[c + 1]), c2, -msc)) : 0.f;
+        lt += e0 + e1;
+        pk[c / 2] = pack_bf16(e0, e1);
+      }
+      l += lt;
+      // the P buffer (and, at the tail, the V rows) are free once P V of the
+      // previous tile is done
+      if (i > 0 && !waited) mbar_wait(bar(kPvDone), (i - 1) & 1, p.err);
+#pragma unroll
+      for (int uq = 0; uq < 4; ++uq)
+        *reinterpret_cast<uint4*>(p_row + ((uq ^ pswz) & 3) * 16) =
+            make_uint4(pk[4 * uq], pk[4 * uq + 1], pk[4 * uq + 2], pk[4 * uq + 3]);
+      if (nvalid < kMlaTile) {
+        // keys past the row limit: zero their V rows (this CTA's 256 dims) so
+        // stale or poisoned cache contents never meet P = 0 in the MMA
+        uint8_t* vst = base + kOffStages + (i % kStages) * kStageBytes + 4 * u.half * kKChunkBytes;
+        const int nz = kMlaTile - max(nvalid, 0);
+        for (int q = row; q < nz * 4 * 8; q += 128) {
+          const int rr = max(nvalid, 0) + q / 32, ch = (q / 8) % 4, un = q % 8;
+          *reinterpret_cast<uint4*>(vst + ch * kKChunkBytes + (rr / 8) * 1024 + (rr % 8) * 128 +
+                                    un * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();  // P and zeroed V rows are read by the MMA (async proxy)
+      tc::fence_before_sync();   // and any in-place O rescale precedes the next P V
+      __syncwarp();
+      named_bar_sync(1, 128);
+      if (row == 0) mbar_arrive(bar(kPFull));
+    }
+
+    // ------------------------------ epilogue ------------------------------
+    if (n > 0) {
+      mbar_wait(bar(kPvDone), (n - 1) & 1, p.err);
+      __syncwarp();  // the TMEM loads below are warp-collective
+      tc::fence_after_sync();
+    }
+    const long long r = (long long)u.b * p.qlen + u.t;
+    uint16_t* out_row = p.out + r * p.o_sr + row * p.o_sh + u.half * kMlaHalf;
+    if (u.nsplit == 1) {
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      for (int j = 0; j < kMlaHalf / 32; ++j) {
+        uint32_t o[32];
+        if (n > 0) {
+          tc::ld_32x32b_x32(tmem + lane_base + kTmemO + 32 * j, o);
+          tc::wait_ld();
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 8) {
+          uint4 v;
+          v.x = n > 0 ? pack_bf16(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv) : 0u;
+          v.y = n > 0 ? pack_bf16(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv) : 0u;
+          v.z = n > 0 ? pack_bf16(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv) : 0u;
+          v.w = n > 0 ? pack_bf16(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv) : 0u;
+          *reinterpret_cast<uint4*>(out_row + 32 * j + c) = v;
+        }
+      }
+      if (u.half == 0)
+        p.lse[r * p.lse_sr + row * p.lse_sh] = (l > 0.f) ? m_used * scale_eff + logf(l) : -INFINITY;
+    } else {
+      // publish the split's partial: O half (fp32), m, l
+      const long long slot = slot_of(p, u, u.split);
+      float* po = p.partials + slot * kMlaPartialFloats + (long long)row * kMlaHalf;
+      for (int j = 0; j < kMlaHalf / 32; ++j) {
+        uint32_t o[32];
+        if (n > 0) {
+          tc::ld_32x32b_x32(tmem + lane_base + kTmemO + 32 * j, o);
+          tc::wait_ld();
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 4)
+          *reinterpret_cast<float4*>(po + 32 * j + c) =
+              n > 0 ? make_float4(__uint_as_float(o[c]), __uint_as_float(o[c + 1]),
+                                  __uint_as_float(o[c + 2]), __uint_as_float(o[c + 3]))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float* pml = p.partials + slot * kMlaPartialFloats + kMlaHeads * kMlaHalf;
+      pml[row] = m_used;
+      pml[kMlaHeads + row] = l;
+      __syncwarp();
+      named_bar_sync(1, 128);
+      int* cnt = p.counters + counter_index(p, u);
+      if (row == 0) *flag = atomic_add_acq_rel_gpu(cnt, 1);
+      __syncwarp();
+      named_bar_sync(1, 128);
+      if (*flag == u.nsplit - 1) {
+        // last split of this (request, token, half): merge every partial
+        float M = -INFINITY;
+        for (int s = 0; s < u.nsplit; ++s)
+          M = fmaxf(M, __ldcg(p.partials + slot_of(p, u, s) * kMlaPartialFloats +
+                              kMlaHeads * kMlaHalf + row));
+        float Ls = 0.f;
+        float w[16];
+        const int ns = u.nsplit;
+        for (int s = 0; s < ns; ++s) {
+          const float* ml = p.partials + slot_of(p, u, s) * kMlaPartialFloats + kMlaHeads * kMlaHalf;
+          const float ms = __ldcg(ml + row);
+          const float ws = (ms == -INFINITY) ? 0.f : ex2((ms - M) * c2);
+          Ls = __fmaf_rn(ws, __ldcg(ml + kMlaHeads + row), Ls);
+          if (s < 16) w[s] = ws;
+        }
+        const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
+        for (int j = 0; j < kMlaHalf; j += 8) {
+          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int s = 0; s < ns; ++s) {
+            const float* src = p.partials + slot_of(p, u, s) * kMlaPartialFloats +
+                               (long long)row * kMlaHalf + j;
+            const float4 a = ldcg_f4(src), bq = ldcg_f4(src + 4);
+            const float ws = w[s];
+            acc[0] = __fmaf_rn(ws, a.x, acc[0]); acc[1] = __fmaf_rn(ws, a.y, acc[1]);
+            acc[2] = __fmaf_rn(ws, a.z, acc[2]); acc[3] = __fmaf_rn(ws, a.w, acc[3]);
+            acc[4] = __fmaf_rn(ws, bq.x, acc[4]); acc[5] = __fmaf_rn(ws, bq.y, acc[5]);
+            acc[6] = __fmaf_rn(ws, bq.z, acc[6]); acc[7] = __fmaf_rn(ws, bq.w, acc[7]);
+          }
+          uint4 v;
+          v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+          v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+          v.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+          v.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+          *reinterpret_cast<uint4*>(out_row + j) = v;
+        }
+        if (u.half == 0)
+          p.lse[r * p.lse_sr + row * p.lse_sh] = (Ls > 0.f) ? M * scale_eff + logf(Ls) : -INFINITY;
+        if (row == 0) store_relaxed_gpu(cnt, 0);
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <bool kFp8>
+cudaError_t launch_t(const MlaParams& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
+                     int grid, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        mla_verify_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  mla_verify_kernel<kFp8><<<grid, kThreads, kSmemBytes, stream>>>(p, q_map, kv_map);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mla_verify(const MlaParams& p, const CUtensorMap& q_map,
+                              const CUtensorMap& kv_map, bool fp8, int grid,
+                              cudaStream_t stream) {
+  (void)fp8;
+  return launch_t<false>(p, q_map, kv_map, grid, stream);
+}
+
+}  // namespace pkv

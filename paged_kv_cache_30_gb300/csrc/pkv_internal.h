@@ -91,6 +91,38 @@ int prepare_gqa_call(const ::pkv_tensor* q, const ::pkv_tensor* kv_cache,
 int abi_fail(int code, const char* message);
 int abi_cuda_fail(cudaError_t e, const char* what);
 
+// ---------------------------------------------------------------- MLA --
+constexpr int kMlaHeads = 128;
+constexpr int kMlaLk = 576;
+constexpr int kMlaLv = 512;
+constexpr int kMlaHalf = kMlaLv / 2;        // output dims per CTA
+constexpr int kMlaTile = 32;                // keys per pipeline tile
+constexpr int kMlaMinTiles = 32;            // a split holds at least 1024 keys
+constexpr int64_t kMlaPartialFloats = int64_t(kMlaHeads) * kMlaHalf + 2 * kMlaHeads;
+
+struct MlaParams {
+  const int32_t* bt;
+  int64_t bt_sb;
+  int max_blocks;
+  int num_pages;
+  const int32_t* seq_lens;
+  const int32_t* real_seq_lens;  // or null
+  const float* k_scale;          // device scalar or null (FP8 only)
+  uint16_t* out;                 // bf16 [B*qlen, 128, 512]
+  int64_t o_sr, o_sh;
+  float* lse;                    // [B*qlen, 128]
+  int64_t lse_sr, lse_sh;
+  int B, qlen, cap, page_size;
+  float scale;
+  float* partials;               // [slots][128*256 + 256]
+  int64_t max_slots;
+  int* counters;                 // [(b*qlen + t)*2 + half]
+  int* err;
+};
+
+cudaError_t launch_mla_verify(const MlaParams& p, const CUtensorMap& q_map,
+                              const CUtensorMap& kv_map, bool fp8, int grid, cudaStream_t stream);
+
 // The counter region of the workspace holds 2^20 ints: the first half for
 // (request, kv head) counters, the second half for split-group counters.
 constexpr int64_t kTopCounters = int64_t(1) << 19;

@@ -12,6 +12,17 @@ TOL_OUT_FP8 = 5e-2
 TOL_LSE = 1e-3
 
 
+def bf16_ulp_diff(a, b):
+    """|a - b| in units of the bf16 ulp at max(|a|, |b|) (elementwise max).
+    Two runs of the same call that only accumulate in a different order
+    differ by at most a couple of these (each side rounds once to bf16)."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    mag = np.maximum(np.maximum(np.abs(a), np.abs(b)), 2.0 ** -100)
+    ulp = 2.0 ** (np.floor(np.log2(mag)) - 7)
+    return float(np.max(np.abs(a - b) / ulp)) if a.size else 0.0
+
+
 def dev(t):
     return None if t is None else t.to("cuda", non_blocking=False)
 

@@ -1,0 +1,155 @@
+"""GPU parity of the MLA causal-verify kernel (tcgen05) against the fp64 oracle,
+through the C ABI (pkv_mla_verify_attn via the ctypes binding)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_30_gb300 as pkv
+from paged_kv_cache_30_gb300 import workloads as W
+from tests.gpu_helpers import TOL_LSE, TOL_OUT, TOL_OUT_FP8, bf16_ulp_diff, compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    pkv.load_library()
+    pkv.init(0)
+
+
+def run_mla(prob, cap=None, dev=None):
+    d = dev or dict(q=prob.q.cuda(), c=prob.latent_cache.cuda(), bt=prob.block_table.cuda(),
+                    sl=prob.seq_lens.cuda(),
+                    rl=None if prob.real_seq_lens is None else prob.real_seq_lens.cuda())
+    R, H, _ = prob.q.shape
+    out = torch.full((R, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((R, H), float("nan"), device="cuda")
+    ks = None
+    if prob.k_scale is not None:
+        ks = torch.tensor(prob.k_scale, dtype=torch.float32, device="cuda")
+    pkv.mla_verify_attn(d["q"], d["c"], d["bt"], d["sl"], d["rl"], prob.qlen, prob.scale,
+                        prob.page_size, ks, out, lse,
+                        prob.num_kv_splits if cap is None else cap)
+    torch.cuda.synchronize()
+    assert pkv.check_errors(0) == 0
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def oracle_mla(prob, rows=None):
+    return oracle.mla_verify(prob.q, prob.latent_cache, prob.block_table, prob.seq_lens,
+                             prob.real_seq_lens, prob.qlen, prob.scale, prob.page_size,
+                             prob.k_scale, rows=rows)
+
+
+def check(prob, cap=None, rows=None, what=""):
+    out, lse = run_mla(prob, cap)
+    ref_out, ref_lse = oracle_mla(prob, rows)
+    R, H, _ = prob.q.shape
+    tol = TOL_OUT_FP8 if prob.k_scale is not None else TOL_OUT
+    if rows is None:
+        return compare(out, lse, ref_out.reshape(R, H, 512), ref_lse.reshape(R, H), tol_out=tol,
+                       what=what)
+    return compare(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse,
+                   tol_out=tol, what=what)
+
+
+def mla_case(seed, L, qlen, P=16, real=None, Lmax=None, has_real=True, cap=0, poison=False):
+    L = np.asarray(L, dtype=np.int32)
+    prob = W.mla_problem(seed, B=len(L), qlen=qlen, H=128, page_size=P, lengths="const",
+                         Lmin=1, Lmax=int(Lmax or max(int(L.max()), 1)), seq_lens=L,
+                         has_real=has_real, num_kv_splits=cap)
+    if real is not None:
+        prob.real_seq_lens = torch.tensor(real, dtype=torch.int32)
+    if poison:
+        bt = prob.block_table.numpy()
+        used = np.zeros(prob.latent_cache.shape[0], dtype=bool)
+        used[bt[bt >= 0]] = True
+        prob.latent_cache[torch.from_numpy(~used)] = float("nan")
+        for b, l in enumerate(L):
+            if l % P:
+                prob.latent_cache[int(bt[b, (l - 1) // P]), l % P:] = float("nan")
+    return prob
+
+
+@pytest.mark.parametrize("seed,L,qlen,P,real,cap", [
+    (0, [1, 31, 32, 33], 1, 16, None, 0),
+    (1, [100, 1000], 4, 16, [97, 1000], 0),
+    (2, [2500, 40, 5], 2, 32, [2500, 38, 0], 2),
+    (3, [4097, 1500], 4, 16, None, 1),
+    (4, [3000, 3000], 3, 16, [2999, 10], 3),
+    (5, [70, 64, 63], 4, 32, None, 16),
+])
+def test_mla_small_cases(seed, L, qlen, P, real, cap):
+    prob = mla_case(seed, L, qlen, P, real=real, cap=cap)
+    check(prob, what=f"mla case {seed}")
+
+
+def test_mla_empty_rows_and_tiny_lengths():
+    # lim = max(min(L - qlen + 1 + t, L_real), 0) is 0 for several rows here
+    prob = mla_case(6, [2, 0, 1, 3], 4, 16, real=[2, 0, 0, 3])
+    out, lse = run_mla(prob)
+    ref_out, ref_lse = oracle_mla(prob)
+    compare(out, lse, ref_out.reshape(out.shape), ref_lse.reshape(lse.shape), what="tiny")
+
+
+def test_mla_poisoned_unattended_slots_stay_finite():
+    prob = mla_case(7, [37, 200, 1025], 4, 16, real=[35, 200, 1024], poison=True)
+    check(prob, what="mla poison")
+
+
+def test_mla_degenerate_warmup_inputs():
+    """All block-table entries point at page 0 and L = qlen (the verify page's
+    warm-up runs every launch variant on such inputs)."""
+    for qlen in (1, 2, 4):
+        prob = mla_case(8, [qlen] * 3, qlen, 16, has_real=False)
+        prob.block_table.zero_()
+        for cap in (1, 2):
+            check(prob, cap, what=f"warmup qlen {qlen} cap {cap}")
+
+
+def test_mla_split_count_invariance():
+    prob = mla_case(9, [6000, 3333], 4, 16, real=[5998, 3333])
+    outs = []
+    for cap in (1, 2, 5, 8, 16):
+        outs.append(run_mla(prob, cap))
+    ref_out, ref_lse = oracle_mla(prob)
+    for out, lse in outs:
+        compare(out, lse, ref_out.reshape(out.shape), ref_lse.reshape(lse.shape), what="inv")
+        # a different split count only reorders fp32 accumulation: within two
+        # bf16 ulps of each other (each side rounds once)
+        assert bf16_ulp_diff(out, outs[0][0]) <= 2.0
+        assert np.max(np.abs(lse - outs[0][1])) <= 3e-4
+
+
+def test_mla_repeated_calls_are_bitwise_identical():
+    prob = mla_case(10, [5000, 2000, 700], 4, 16)
+    d = dict(q=prob.q.cuda(), c=prob.latent_cache.cuda(), bt=prob.block_table.cuda(),
+             sl=prob.seq_lens.cuda(), rl=prob.real_seq_lens.cuda())
+    first = run_mla(prob, dev=d)
+    for _ in range(20):
+        again = run_mla(prob, dev=d)
+        assert np.array_equal(first[0], again[0]) and np.array_equal(first[1], again[1])
+    assert pkv.check_counters(0) == 0
+
+
+def test_mla_verify_b32_full_size_sampled_rows():
+    """B=32, qlen=4, H=128, L ~ U[512, 8192], L_real = L - U[0,3], cap 8: the
+    whole launch on the GPU, 1024 sampled rows against the oracle."""
+    prob = W.mla_verify(0)
+    rows = np.random.default_rng(1).choice(32 * 4 * 128, size=1024, replace=False)
+    check(prob, rows=rows, what="mla config b32 q4")
+
+
+def test_mla_fp8_cache_not_built_yet_is_reported():
+    prob = mla_case(11, [64], 1, 16)
+    c8 = prob.latent_cache.float().to(torch.float8_e4m3fn).cuda()
+    out = torch.empty((1, 128, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 128), device="cuda")
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.mla_verify_attn(prob.q.cuda(), c8, prob.block_table.cuda(), prob.seq_lens.cuda(),
+                            None, 1, prob.scale, 16,
+                            torch.tensor(0.05, device="cuda"), out, lse)
+    assert ei.value.code == -2
