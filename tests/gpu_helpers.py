@@ -12,15 +12,16 @@ TOL_OUT_FP8 = 5e-2
 TOL_LSE = 1e-3
 
 
-def bf16_ulp_diff(a, b):
-    """|a - b| in units of the bf16 ulp at max(|a|, |b|) (elementwise max).
-    Two runs of the same call that only accumulate in a different order
-    differ by at most a couple of these (each side rounds once to bf16)."""
+def within_bf16_reorder(a, b, ulps=2.0, floor=1e-4):
+    """True when two runs of one call that only accumulate in a different
+    order agree: each element within `ulps` bf16 ulps of the larger magnitude
+    (each side rounds once to bf16), or within `floor` absolute for values
+    near zero, where fp32 cancellation (terms of size ~1) dominates."""
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     mag = np.maximum(np.maximum(np.abs(a), np.abs(b)), 2.0 ** -100)
     ulp = 2.0 ** (np.floor(np.log2(mag)) - 7)
-    return float(np.max(np.abs(a - b) / ulp)) if a.size else 0.0
+    return bool(np.all(np.abs(a - b) <= np.maximum(ulps * ulp, floor)))
 
 
 def dev(t):
