@@ -533,7 +533,6 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
     return fail(PKV_ERR_ALIGNMENT, "q and out must be 16-byte aligned with strides % 8 == 0");
   if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
   if (num_kv_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_splits < 0");
-  if (fp8) return fail(PKV_ERR_UNSUPPORTED, "the FP8 latent cache path is not built yet");
   if (B == 0) return PKV_OK;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
@@ -572,8 +571,11 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
     const cuuint64_t gstr[2] = {cuuint64_t(s_tok) * esz, cuuint64_t(s_page) * esz};
     const cuuint32_t box[3] = {64, 16, 1};
     const cuuint32_t es[3] = {1, 1, 1};
-    CUresult cr = encode(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, latent_cache->data, gdim,
-                         gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    // bf16: 128-byte rows swizzled for the MMA; e4m3: 64-byte rows, plain (converted in smem)
+    CUresult cr = encode(&kv_map,
+                         fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                         latent_cache->data, gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS)
       return fail(PKV_ERR_INVALID_ARG, "latent cache tensor map rejected (%d)", (int)cr);

@@ -31,24 +31,38 @@
 #include "ptx.cuh"
 #include "tcgen05.cuh"
 
+#include <cuda_fp16.h>
+
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 256;
 constexpr int kSoftmaxWarp0 = 4;
-constexpr int kStages = 2;
 constexpr int kChunks = kMlaLk / 64;            // 9 64-dim chunks of a latent row
 constexpr int kQChunkBytes = kMlaHeads * 128;   // 16 KB: 128 rows x 64 dims
-constexpr int kKChunkBytes = kMlaTile * 128;    // 4 KB: 32 keys x 64 dims
+constexpr int kKChunkBytes = kMlaTile * 128;    // 4 KB: 32 keys x 64 dims (bf16)
 constexpr int kQBytes = kChunks * kQChunkBytes;     // 147456
-constexpr int kStageBytes = kChunks * kKChunkBytes; // 36864
+constexpr int kStageBytes = kChunks * kKChunkBytes; // 36864: one bf16 tile
+constexpr int kF8StageBytes = kStageBytes / 2;      // 18432: one e4m3 tile
+constexpr int kF8BoxBytes = 16 * 64;                // 16 keys x 64 dims of e4m3
 constexpr int kPBytes = kMlaHeads * kMlaTile * 2;   // 8192 (64-byte rows)
-constexpr int kOffStages = kQBytes;
-constexpr int kOffP = kOffStages + kStages * kStageBytes;
-constexpr int kOffBars = kOffP + kPBytes;
-constexpr int kSmemBytes = kOffBars + 128 + 1024;
-static_assert(kOffStages % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1024 B alignment");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+// Shared memory: [Q | bf16 tile stages | e4m3 tile stages (FP8 only) | P | barriers].
+// The bf16 path double-buffers its bf16 tiles; the FP8 path double-buffers the
+// e4m3 tiles that TMA lands and converts each into a single bf16 stage.
+template <bool kFp8>
+struct Cfg {
+  static constexpr int kThreads = kFp8 ? 384 : 256;  // FP8: warps 2, 3, 8..11 convert
+  static constexpr int kStages = kFp8 ? 1 : 2;
+  static constexpr int kF8Stages = kFp8 ? 2 : 0;
+  static constexpr int kOffStages = kQBytes;
+  static constexpr int kOffF8 = kOffStages + kStages * kStageBytes;
+  static constexpr int kOffP = kOffF8 + kF8Stages * kF8StageBytes;
+  static constexpr int kOffBars = kOffP + kPBytes;
+  static constexpr int kSmemBytes = kOffBars + 256 + 1024;
+  static_assert(kOffStages % 1024 == 0 && kOffF8 % 1024 == 0 && kOffP % 1024 == 0,
+                "swizzle atoms need 1024 B alignment");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;     // columns [0, 256): O half
@@ -58,7 +72,8 @@ constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 
 
 // barrier indices
 enum { kQFull = 0, kKvFull = 1, kKvEmpty = 3, kSFull = 5, kSFree = 7, kPFull = 9, kPvDone = 10,
-       kNumBars = 11 };
+       kF8Full = 11, kF8Empty = 13, kBfFull = 15, kBfFree = 16, kNumBars = 17 };
+constexpr int kConverters = 192;  // FP8: six converter warps
 
 struct Unit {
   int b, split, t, half, nsplit;
@@ -105,9 +120,11 @@ __device__ __forceinline__ long long slot_of(const MlaParams& p, const Unit& u, 
 }
 
 template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     mla_verify_kernel(const __grid_constant__ MlaParams p, const __grid_constant__ CUtensorMap q_map,
                       const __grid_constant__ CUtensorMap kv_map) {
+  using C = Cfg<kFp8>;
+  constexpr int kStages = C::kStages;
   const Unit u = decode_unit(p);
   if (u.split >= u.nsplit) return;  // this request needs fewer splits
 
@@ -115,23 +132,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u32 - raw_u32);
-  const uint32_t sQ = base_u32, sK = base_u32 + kOffStages, sP = base_u32 + kOffP;
-  const uint32_t bars = base_u32 + kOffBars;
+  const uint32_t sQ = base_u32, sK = base_u32 + C::kOffStages, sP = base_u32 + C::kOffP;
+  const uint32_t sF8 = base_u32 + C::kOffF8;
+  const uint32_t bars = base_u32 + C::kOffBars;
   auto bar = [&](int i) { return bars + 8u * i; };
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + kOffBars + 8 * kNumBars);
-  int* flag = reinterpret_cast<int*>(base + kOffBars + 8 * kNumBars + 16);
+  volatile uint32_t* tmem_slot =
+      reinterpret_cast<volatile uint32_t*>(base + C::kOffBars + 8 * kNumBars);
+  int* flag = reinterpret_cast<int*>(base + C::kOffBars + 8 * kNumBars + 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     mbar_init(bar(kQFull), 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < 2; ++s) {  // every barrier either path may touch
       mbar_init(bar(kKvFull + s), 1);
       mbar_init(bar(kKvEmpty + s), 1);
-      mbar_init(bar(kSFull + s), 1);
+      mbar_init(bar(kSFull + s), 1);   // two score buffers on both paths
       mbar_init(bar(kSFree + s), 128);
     }
     mbar_init(bar(kPFull), 1);
     mbar_init(bar(kPvDone), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kF8Full + s), 1);
+      mbar_init(bar(kF8Empty + s), 1);
+    }
+    mbar_init(bar(kBfFull), 1);
+    mbar_init(bar(kBfFree), 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -142,8 +167,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  float scale_eff = p.scale;
-  if (kFp8 && p.k_scale) scale_eff *= __ldg(p.k_scale);
+  float scale_eff = p.scale, out_scale = 1.f;
+  if (kFp8 && p.k_scale) {
+    out_scale = __ldg(p.k_scale);  // V = raw e4m3 x k_scale
+    scale_eff *= out_scale;
+  }
   const float c2 = scale_eff * kLog2e;
   const int n = u.ntiles;
 
@@ -172,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int o0 = __shfl_sync(0xffffffffu, off, 2 * (i - g));
           const int b1 = __shfl_sync(0xffffffffu, blk, 2 * (i - g) + 1);
           const int o1 = __shfl_sync(0xffffffffu, off, 2 * (i - g) + 1);
-          if (lane == 0) {
+          if (lane == 0 && !kFp8) {
             const int st = i % kStages;
             mbar_wait(bar(kKvEmpty + st), ((i / kStages) & 1) ^ 1u, p.err);
             mbar_arrive_expect_tx(bar(kKvFull + st), kStageBytes);
@@ -181,6 +209,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d(dst + c * kKChunkBytes, &kv_map, bar(kKvFull + st), 64 * c, o0, b0);
               tma_load_3d(dst + c * kKChunkBytes + 2048, &kv_map, bar(kKvFull + st), 64 * c, o1,
                           b1);
+            }
+          } else if (lane == 0) {
+            // e4m3 boxes of 16 keys x 64 dims, unswizzled: box (piece h, chunk c)
+            // at (h * 9 + c) * 1 KB, 64-byte rows
+            const int st = i & 1;
+            mbar_wait(bar(kF8Empty + st), ((i >> 1) & 1) ^ 1u, p.err);
+            mbar_arrive_expect_tx(bar(kF8Full + st), kF8StageBytes);
+            const uint32_t dst = sF8 + st * kF8StageBytes;
+            for (int c = 0; c < kChunks; ++c) {
+              tma_load_3d(dst + c * kF8BoxBytes, &kv_map, bar(kF8Full + st), 64 * c, o0, b0);
+              tma_load_3d(dst + (kChunks + c) * kF8BoxBytes, &kv_map, bar(kF8Full + st), 64 * c,
+                          o1, b1);
             }
           }
         }
@@ -202,11 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                        tc::smem_desc(v0 + ks * 2048, kKChunkBytes, 1024, tc::kSwizzle128), id_pv,
                        j > 0 || ks > 0);
         tc::commit(bar(kPvDone));
-        tc::commit(bar(kKvEmpty + j % kStages));
+        tc::commit(bar(kFp8 ? kBfFree : kKvEmpty + j % kStages));
       };
       for (int i = 0; i < n; ++i) {
         const int st = i % kStages, sb = i & 1;
-        mbar_wait(bar(kKvFull + st), (i / kStages) & 1, p.err);
+        if (kFp8)
+          mbar_wait(bar(kBfFull), i & 1, p.err);
+        else
+          mbar_wait(bar(kKvFull + st), (i / kStages) & 1, p.err);
         mbar_wait(bar(kSFree + sb), ((i >> 1) & 1) ^ 1u, p.err);
         tc::fence_after_sync();
         const uint32_t kst = sK + st * kStageBytes;
@@ -219,16 +262,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                          id_s, (c | ks) != 0);
         }
         tc::commit(bar(kSFull + sb));
-        if (i > 0) do_pv(i - 1);
+        if (kFp8) {
+          do_pv(i);  // the single bf16 stage is converted again only after P V
+        } else if (i > 0) {
+          do_pv(i - 1);
+        }
       }
-      do_pv(n - 1);
+      if (!kFp8) do_pv(n - 1);
     }
-  } else if (warp >= kSoftmaxWarp0) {
+  } else if (kFp8 && (warp == 2 || warp == 3 || warp >= 8)) {
+    // ============ FP8: e4m3 tile -> bf16 tile in the MMA's swizzled layout ============
+    // Exact: every e4m3 value is a bf16 value.  k_scale is applied to the scores
+    // and to the output instead.
+    const int ct = (warp < 8) ? tid - 64 : tid - 256 + 64;  // 0 .. 191
+    for (int i = 0; i < n; ++i) {
+      const int st = i & 1;
+      mbar_wait(bar(kF8Full + st), (i >> 1) & 1, p.err);
+      if (i > 0) mbar_wait(bar(kBfFree), (i - 1) & 1, p.err);  // P V of tile i-1 is done
+      const uint8_t* src = base + C::kOffF8 + st * kF8StageBytes;
+      uint8_t* dst = base + C::kOffStages;
+      // 1152 items: (piece h, chunk c, key row rr of 16, 16-byte e4m3 unit q of 4)
+      for (int it = ct; it < 2 * kChunks * 16 * 4; it += kConverters) {
+        const int q = it & 3, rr = (it >> 2) & 15, hc = it >> 6;  // hc = h * 9 + c
+        const int h = hc / kChunks, c = hc % kChunks;
+        const uint4 w = *reinterpret_cast<const uint4*>(src + hc * kF8BoxBytes + rr * 64 + q * 16);
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint16_t pair = (uint16_t)(wv[k] >> (16 * hh));
+            uint32_t f16x2;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
+            const __half2 hv = *reinterpret_cast<const __half2*>(&f16x2);
+            const float2 fv = __half22float2(hv);
+            o[2 * k + hh] = pack_bf16(fv.x, fv.y);
+          }
+        }
+        const int row = 16 * h + rr;  // key row of the tile
+        uint8_t* rowp = dst + c * kKChunkBytes + (row / 8) * 1024 + (row % 8) * 128;
+        // e4m3 unit q holds dims 16q .. 16q + 15 = bf16 units 2q, 2q + 1
+        *reinterpret_cast<uint4*>(rowp + (((2 * q) ^ (row % 8)) * 16)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(rowp + (((2 * q + 1) ^ (row % 8)) * 16)) =
+            make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      fence_proxy_async_smem();  // the MMA reads the bf16 tile through the async proxy
+      __syncwarp();
+      named_bar_sync(2, kConverters);
+      if (ct == 0) {
+        mbar_arrive(bar(kF8Empty + st));
+        mbar_arrive(bar(kBfFull));
+      }
+    }
+  } else if (warp >= kSoftmaxWarp0 && warp < 8) {
     // ================= softmax (one thread per head) + epilogue ============
     const int row = tid - kSoftmaxWarp0 * 32;           // head 0..127
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     float m_used = -INFINITY, l = 0.f;
-    uint8_t* p_row = base + kOffP + (row / 8) * 512 + (row % 8) * 64;
+    uint8_t* p_row = base + C::kOffP + (row / 8) * 512 + (row % 8) * 64;
     const int pswz = (row % 8) >> 1;
     for (int i = 0; i < n; ++i) {
       const int sb = i & 1;
@@ -299,7 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nvalid < kMlaTile) {
         // keys past the row limit: zero their V rows (this CTA's 256 dims) so
         // stale or poisoned cache contents never meet P = 0 in the MMA
-        uint8_t* vst = base + kOffStages + (i % kStages) * kStageBytes + 4 * u.half * kKChunkBytes;
+        uint8_t* vst =
+            base + C::kOffStages + (i % kStages) * kStageBytes + 4 * u.half * kKChunkBytes;
         const int nz = kMlaTile - max(nvalid, 0);
         for (int q = row; q < nz * 4 * 8; q += 128) {
           const int rr = max(nvalid, 0) + q / 32, ch = (q / 8) % 4, un = q % 8;
@@ -323,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long r = (long long)u.b * p.qlen + u.t;
     uint16_t* out_row = p.out + r * p.o_sr + row * p.o_sh + u.half * kMlaHalf;
     if (u.nsplit == 1) {
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      const float inv = (l > 0.f) ? out_scale / l : 0.f;
       for (int j = 0; j < kMlaHalf / 32; ++j) {
         uint32_t o[32];
         if (n > 0) {
@@ -384,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           Ls = __fmaf_rn(ws, __ldcg(ml + kMlaHeads + row), Ls);
           if (s < 16) w[s] = ws;
         }
-        const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
+        const float inv = (Ls > 0.f) ? out_scale / Ls : 0.f;
         for (int j = 0; j < kMlaHalf; j += 8) {
           float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
           for (int s = 0; s < ns; ++s) {
@@ -426,11 +520,12 @@ cudaError_t launch_t(const MlaParams& p, const CUtensorMap& q_map, const CUtenso
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e = cudaFuncSetAttribute(
-        mla_verify_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        mla_verify_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kFp8>::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  mla_verify_kernel<kFp8><<<grid, kThreads, kSmemBytes, stream>>>(p, q_map, kv_map);
+  mla_verify_kernel<kFp8><<<grid, Cfg<kFp8>::kThreads, Cfg<kFp8>::kSmemBytes, stream>>>(p, q_map,
+                                                                                       kv_map);
   return cudaGetLastError();
 }
 
@@ -439,8 +534,8 @@ cudaError_t launch_t(const MlaParams& p, const CUtensorMap& q_map, const CUtenso
 cudaError_t launch_mla_verify(const MlaParams& p, const CUtensorMap& q_map,
                               const CUtensorMap& kv_map, bool fp8, int grid,
                               cudaStream_t stream) {
-  (void)fp8;
-  return launch_t<false>(p, q_map, kv_map, grid, stream);
+  return fp8 ? launch_t<true>(p, q_map, kv_map, grid, stream)
+             : launch_t<false>(p, q_map, kv_map, grid, stream);
 }
 
 }  // namespace pkv

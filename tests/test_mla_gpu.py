@@ -148,13 +148,24 @@ def test_mla_verify_b32_full_size_sampled_rows():
     check(prob, rows=rows, what="mla config b32 q4")
 
 
-def test_mla_fp8_cache_not_built_yet_is_reported():
-    prob = mla_case(11, [64], 1, 16)
-    c8 = prob.latent_cache.float().to(torch.float8_e4m3fn).cuda()
-    out = torch.empty((1, 128, 512), dtype=torch.bfloat16, device="cuda")
-    lse = torch.empty((1, 128), device="cuda")
-    with pytest.raises(pkv.PkvError) as ei:
-        pkv.mla_verify_attn(prob.q.cuda(), c8, prob.block_table.cuda(), prob.seq_lens.cuda(),
-                            None, 1, prob.scale, 16,
-                            torch.tensor(0.05, device="cuda"), out, lse)
-    assert ei.value.code == -2
+@pytest.mark.parametrize("seed,L,qlen,real,k_scale,cap", [
+    (11, [64, 1, 1500], 1, None, 0.05, 0),
+    (12, [3000, 33], 4, [2998, 33], 0.05, 2),
+    (13, [700, 2049], 2, None, 0.125, 16),
+])
+def test_mla_fp8_small_cases(seed, L, qlen, real, k_scale, cap):
+    L = np.asarray(L, dtype=np.int32)
+    prob = W.mla_problem(seed, B=len(L), qlen=qlen, H=128, page_size=16, lengths="const",
+                         Lmin=1, Lmax=int(L.max()), seq_lens=L, fp8=True, k_scale=k_scale,
+                         has_real=real is not None, num_kv_splits=cap)
+    if real is not None:
+        prob.real_seq_lens = torch.tensor(real, dtype=torch.int32)
+    check(prob, what=f"fp8 case {seed}")
+
+
+def test_mla_fp8_b128_full_size_sampled_rows():
+    """B=128, qlen=1, H=128, e4m3 latent cache holding N(0,1)/k_scale, k_scale
+    0.05, log-uniform L in [1, 32768], cap 16: 1024 sampled rows."""
+    prob = W.mla_fp8(0)
+    rows = np.random.default_rng(2).choice(128 * 128, size=1024, replace=False)
+    check(prob, rows=rows, what="mla fp8 b128")
