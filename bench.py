@@ -62,6 +62,15 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def measured_bf16_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def profiled_traffic():
     """DRAM bytes per launch of the full-layer kernel from the committed ncu
     summary, if it was taken on the current kernel source (else None)."""
@@ -181,6 +190,124 @@ def oracle_baseline(layers, budget_s: float, threads: int):
         groups += 1
         i += 1
     return done_bytes / t_used / 1e9, t_used, groups
+
+
+# ---------------------------------------------------- the other workloads ---
+def mla_flops(prob) -> float:
+    """Algorithmic MLA flops: every (row, head) attends lim keys with a 576-wide
+    Q.K and a 512-wide P.V (2 flops per multiply-add).  The row limit is the
+    verify page's max(min(L - qlen + 1 + t, L_real), 0), restated here for the
+    count."""
+    import numpy as np
+    L = prob.seq_lens.numpy().astype(np.int64)
+    Lr = L if prob.real_seq_lens is None else prob.real_seq_lens.numpy().astype(np.int64)
+    tot = 0
+    for t in range(prob.qlen):
+        lim = np.maximum(np.minimum(L - prob.qlen + 1 + t, Lr), 0)
+        tot += int(lim.sum())
+    return float(tot) * 128 * 2 * (576 + 512)
+
+
+def time_events(fn, flush, steps, warmup=3):
+    import torch
+    for _ in range(warmup):
+        fn()
+        flush.fill_(1.0)
+    ev = []
+    for s in range(steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        flush.fill_(float(s & 7))
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    ms = sorted(x.elapsed_time(y) for x, y in ev)
+    return statistics.median(ms), statistics.mean(ms)
+
+
+def other_workloads(dev, flush, peak_hbm, peak_tf, steps):
+    """Every other workload of the pages' problem, timed the same way (inputs
+    resident, L2 flushed between calls, CUDA events): the tiny decode batch,
+    the 131072-token long context at B=1 and B=8 across split caps, and the
+    two MLA verify workloads (bf16 and FP8 latent caches)."""
+    import torch
+    import paged_kv_cache_30_gb300 as pkv
+    from paged_kv_cache_30_gb300 import workloads as W
+    res = {}
+
+    def gqa_entry(prob, caps):
+        t = dict(q=prob.q.to(dev), kv=prob.kv_cache.to(dev), bt=prob.block_table.to(dev),
+                 sl=prob.seq_lens.to(dev),
+                 sk=None if prob.sinks is None else prob.sinks.to(dev))
+        out = torch.empty_like(t["q"])
+        lse = torch.empty(t["q"].shape[:2], device=dev)
+        nbytes = prob.kv_bytes()
+        out_d = {"kv_bytes": nbytes}
+        for cap in caps:
+            fn = lambda: pkv.paged_decode_attn(t["q"], t["kv"], t["bt"], t["sl"], t["sk"],
+                                               prob.window, prob.scale, prob.page_size, cap, out,
+                                               lse)
+            med, _ = time_events(fn, flush, steps)
+            out_d[f"cap_{cap}"] = {"us": 1e3 * med, "GBps": nbytes / (med * 1e-3) / 1e9,
+                                   "hbm_frac_of_measured": nbytes / (med * 1e-3) / 1e9 / peak_hbm}
+        del t
+        return out_d, (prob, out, lse)
+
+    # tiny decode batch: latency-bound, report calls/s eager and as CUDA-graph replay
+    tiny = W.tiny_gqa(0)
+    d, (prob, out, lse) = gqa_entry(tiny, [4])
+    t = dict(q=tiny.q.to(dev), kv=tiny.kv_cache.to(dev), bt=tiny.block_table.to(dev),
+             sl=tiny.seq_lens.to(dev))
+    s = torch.cuda.Stream()
+    call = lambda: pkv.paged_decode_attn(t["q"], t["kv"], t["bt"], t["sl"], None, 0, tiny.scale,
+                                         16, 4, out, lse, stream=s)
+    with torch.cuda.stream(s):
+        call()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(100):
+            call()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(10):
+        g.replay()
+    b.record(s)
+    torch.cuda.synchronize()
+    d["graph_replay_calls_per_s"] = 1000 / (a.elapsed_time(b) * 1e-3)  # 10 x 100 calls
+    d["eager_calls_per_s"] = 1e6 / d["cap_4"]["us"]
+    res["tiny_gqa_b4"] = d
+
+    for B in (1, 8):
+        prob = W.long_context(0, B=B)
+        res[f"long_ctx_b{B}"], _ = gqa_entry(prob, [0, 1, 8, 32, 132])
+        del prob
+
+    for name, prob in (("mla_verify_b32_q4", W.mla_verify(0)), ("mla_fp8_b128", W.mla_fp8(0))):
+        tq = prob.q.to(dev)
+        tc = prob.latent_cache.to(dev)
+        tbt, tsl = prob.block_table.to(dev), prob.seq_lens.to(dev)
+        trl = None if prob.real_seq_lens is None else prob.real_seq_lens.to(dev)
+        ks = None if prob.k_scale is None else torch.tensor(prob.k_scale, device=dev)
+        out = torch.empty((tq.shape[0], 128, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((tq.shape[0], 128), device=dev)
+        fn = lambda: pkv.mla_verify_attn(tq, tc, tbt, tsl, trl, prob.qlen, prob.scale,
+                                         prob.page_size, ks, out, lse, prob.num_kv_splits)
+        med, _ = time_events(fn, flush, steps)
+        fl = mla_flops(prob)
+        nbytes = prob.kv_bytes()
+        res[name] = {"us": 1e3 * med, "TFLOPs": fl / (med * 1e-3) / 1e12,
+                     "tensor_frac_of_measured_bf16": fl / (med * 1e-3) / 1e12 / peak_tf,
+                     "GBps": nbytes / (med * 1e-3) / 1e9, "flops": fl, "kv_bytes": nbytes,
+                     "cap": prob.num_kv_splits}
+        del tq, tc
+    assert pkv.check_errors(dev.index or 0) == 0
+    return res
 
 
 # ------------------------------------------------------------- reference ---
@@ -370,6 +497,10 @@ def run_gpu(args, rank, world, local_rank):
                          f"(longest requests first, all 8 query heads each), "
                          f"{t_used:.1f} s of fp64 oracle work on {threads} threads"}
 
+    extra = None
+    if world == 1 and not args.no_extra:
+        extra = other_workloads(dev, flush, peak, measured_bf16_tflops(), args.extra_steps)
+
     clocks = sampler.summary(t0, t1)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -390,6 +521,7 @@ def run_gpu(args, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
+        "other_workloads": extra,
         "clocks": clocks,
         "kernel_hash": kernel_hash(),
     }
@@ -407,6 +539,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads (tiny, long context, MLA)")
+    ap.add_argument("--extra-steps", type=int, default=30)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
