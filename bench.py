@@ -40,8 +40,7 @@ WORKLOAD = ("flint_gqa_b64: B=64, Hq=64, Hkv=8, head_dim=128, bf16 HND pages of 
             "full-attention layer + one sliding-window-128 layer per step")
 FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 KERNEL_SOURCES = ["paged_kv_cache_30_gb300/csrc/gqa_decode.cu",
-                  "paged_kv_cache_30_gb300/csrc/ptx.cuh",
-                  "paged_kv_cache_30_gb300/csrc/pkv_internal.h"]
+                  "paged_kv_cache_30_gb300/csrc/ptx.cuh"]
 
 
 def kernel_hash() -> str:
@@ -227,7 +226,37 @@ def time_events(fn, flush, steps, warmup=3):
     return statistics.median(ms), statistics.mean(ms)
 
 
-def other_workloads(dev, flush, peak_hbm, peak_tf, steps):
+def _tiny(dev, flush, steps, tiny, gqa_entry):
+    import torch
+    import paged_kv_cache_30_gb300 as pkv
+    d, (prob, out, lse) = gqa_entry(tiny, [4])
+    t = dict(q=tiny.q.to(dev), kv=tiny.kv_cache.to(dev), bt=tiny.block_table.to(dev),
+             sl=tiny.seq_lens.to(dev))
+    s = torch.cuda.Stream()
+    call = lambda: pkv.paged_decode_attn(t["q"], t["kv"], t["bt"], t["sl"], None, 0, tiny.scale,
+                                         16, 4, out, lse, stream=s)
+    with torch.cuda.stream(s):
+        call()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(100):
+            call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):  # replay and both events on one stream
+        g.replay()
+        a.record(s)
+        for _ in range(10):
+            g.replay()
+        b.record(s)
+    torch.cuda.synchronize()
+    d["graph_replay_calls_per_s"] = 1000 / (a.elapsed_time(b) * 1e-3)  # 10 x 100 calls
+    d["eager_calls_per_s"] = 1e6 / d["cap_4"]["us"]
+    return d
+
+
+def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
     """Every other workload of the pages' problem, timed the same way (inputs
     resident, L2 flushed between calls, CUDA events): the tiny decode batch,
     the 131072-token long context at B=1 and B=8 across split caps, and the
@@ -255,40 +284,22 @@ def other_workloads(dev, flush, peak_hbm, peak_tf, steps):
         del t
         return out_d, (prob, out, lse)
 
+    want = (lambda k: only is None or k in only)
     # tiny decode batch: latency-bound, report calls/s eager and as CUDA-graph replay
-    tiny = W.tiny_gqa(0)
-    d, (prob, out, lse) = gqa_entry(tiny, [4])
-    t = dict(q=tiny.q.to(dev), kv=tiny.kv_cache.to(dev), bt=tiny.block_table.to(dev),
-             sl=tiny.seq_lens.to(dev))
-    s = torch.cuda.Stream()
-    call = lambda: pkv.paged_decode_attn(t["q"], t["kv"], t["bt"], t["sl"], None, 0, tiny.scale,
-                                         16, 4, out, lse, stream=s)
-    with torch.cuda.stream(s):
-        call()
-    s.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        for _ in range(100):
-            call()
-    torch.cuda.synchronize()
-    g.replay()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(s)
-    for _ in range(10):
-        g.replay()
-    b.record(s)
-    torch.cuda.synchronize()
-    d["graph_replay_calls_per_s"] = 1000 / (a.elapsed_time(b) * 1e-3)  # 10 x 100 calls
-    d["eager_calls_per_s"] = 1e6 / d["cap_4"]["us"]
-    res["tiny_gqa_b4"] = d
-
+    if want("tiny"):
+        res["tiny_gqa_b4"] = _tiny(dev, flush, steps, W.tiny_gqa(0), gqa_entry)
     for B in (1, 8):
+        if not want(f"long{B}"):
+            continue
         prob = W.long_context(0, B=B)
         res[f"long_ctx_b{B}"], _ = gqa_entry(prob, [0, 1, 8, 32, 132])
         del prob
 
-    for name, prob in (("mla_verify_b32_q4", W.mla_verify(0)), ("mla_fp8_b128", W.mla_fp8(0))):
+    for key, name, mk in (("mla", "mla_verify_b32_q4", W.mla_verify),
+                          ("mla_fp8", "mla_fp8_b128", W.mla_fp8)):
+        if not want(key):
+            continue
+        prob = mk(0)
         tq = prob.q.to(dev)
         tc = prob.latent_cache.to(dev)
         tbt, tsl = prob.block_table.to(dev), prob.seq_lens.to(dev)
@@ -382,6 +393,16 @@ def run_gpu(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
+
+    if args.only:
+        # profiling aid: time only the named other workloads
+        flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        peak, _ = measured_peaks()
+        res = other_workloads(dev, flush, peak, measured_bf16_tflops(), args.extra_steps,
+                              only=set(args.only.split(",")))
+        if rank == 0:
+            print(json.dumps({"other_workloads": res}), flush=True)
+        return
 
     # weak scaling: every rank runs its own batch of 64 requests
     layers = make_layers(args.seed + 7919 * rank)
@@ -542,6 +563,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other workloads (tiny, long context, MLA)")
     ap.add_argument("--extra-steps", type=int, default=30)
+    ap.add_argument("--only", default="",
+                    help="comma list of tiny,long1,long8,mla,mla_fp8: time only these (no headline)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
