@@ -401,7 +401,7 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
 
   EncodeTiledFn encode = nullptr;
   if ((rc = get_encoder(&encode))) return rc;
-  alignas(64) CUtensorMap map;
+  CUtensorMap map;
   const cuuint64_t gdim[4] = {cuuint64_t(2 * D), cuuint64_t(page_size), cuuint64_t(Hkv),
                               cuuint64_t(nb)};
   const cuuint64_t gstride[3] = {cuuint64_t(kv_cache->stride[2]) * 2,
@@ -442,7 +442,7 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
   p.min_pages = 256 / page_size;  // a split streams at least 256 tokens (128 KB per kv head)
   const int64_t grid64 = std::min<int64_t>(int64_t(ws.num_sms) * pkv::gqa_ctas_per_sm(), bh * cap);
   const int grid = int(grid64 < 1 ? 1 : grid64);
-  p.target_items = grid * 12;
+  p.target_items = grid * 4;  // about four items per CTA (A/B on GB300: best of 2..24)
   p.part_o = ws.partials;
   p.part_ml = ws.partials + max_items * pkv::kGqaPartialFloats;
   p.max_items = max_items;
@@ -555,7 +555,7 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
 
   EncodeTiledFn encode = nullptr;
   if ((rc = get_encoder(&encode))) return rc;
-  alignas(64) CUtensorMap q_map, kv_map;
+  CUtensorMap q_map, kv_map;
   {
     const cuuint64_t gdim[3] = {cuuint64_t(Lk), cuuint64_t(H), cuuint64_t(R)};
     const cuuint64_t gstr[2] = {cuuint64_t(q->stride[1]) * 2, cuuint64_t(q->stride[0]) * 2};

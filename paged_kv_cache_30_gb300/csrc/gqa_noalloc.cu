@@ -99,7 +99,7 @@ extern "C" PKV_API int pkv_paged_decode_attn_noalloc(
   const int64_t grid64 =
       std::min<int64_t>(int64_t(st.num_sms) * pkv::gqa_ctas_per_sm(), call.pairs * cap);
   const int grid = int(grid64 < 1 ? 1 : grid64);
-  p.target_items = grid * 12;
+  p.target_items = grid * 4;  // about four items per CTA (A/B on GB300: best of 2..24)
 
   // The array keeps the previous call's contents: the queue words and every
   // arrival counter must start this call at zero.

@@ -76,7 +76,7 @@ int gqa_ctas_per_sm();
 // and the KV-cache tensor map.
 struct GqaCall {
   GqaParams p;
-  alignas(64) CUtensorMap map;
+  CUtensorMap map;  // CUtensorMap carries its own 64-byte alignment
   int64_t pairs;   // B * Hkv
   int cap_req;     // num_kv_splits as given (0 = library's choice)
   int page_size;
