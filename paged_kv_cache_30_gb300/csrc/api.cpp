@@ -542,7 +542,7 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
   if ((rc = workspace_for(stream, &dev, &st, &capturing))) return rc;
   const pkv::Workspace& ws = st->ws;
   // splits: at most 16 per (request, token, half); the device uses fewer for
-  // short requests (at least 1024 keys per split)
+  // short requests (at least 4096 keys per split)
   int64_t cap = num_kv_splits == 0 ? 16 : std::min<int64_t>(num_kv_splits, 16);
   const int64_t max_slots = int64_t(ws.partial_bytes) / (pkv::kMlaPartialFloats * 4);
   const int64_t units = B * qlen * 2;
@@ -582,6 +582,12 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
   }
   pkv::MlaParams p;
   std::memset(&p, 0, sizeof p);
+  p.q = static_cast<const uint16_t*>(q->data);
+  p.q_sr = q->stride[0];
+  p.q_sh = q->stride[1];
+  p.kv = static_cast<const uint8_t*>(latent_cache->data);
+  p.kv_stok = s_tok * esz;
+  p.kv_spage = s_page * esz;
   p.bt = static_cast<const int32_t*>(block_table->data);
   p.bt_sb = block_table->stride[0];
   p.max_blocks = int(std::min<int64_t>(block_table->shape[1], int64_t(1) << 30));

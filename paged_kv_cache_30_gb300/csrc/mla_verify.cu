@@ -11,19 +11,25 @@
 //
 // One CTA per (request, split, verify token, half of the 512 output dims);
 // inactive splits return at once.  Tensor memory (512 columns) holds the
-// CTA's output half O[128 x 256] (fp32) and two score buffers S[128 x 32].
-//   warp 0      TMA: the token's 128 x 576 query tile once, then 32-key tiles
-//               of the latent cache (9 boxes of 64 dims per 16-token page
-//               piece, 128-byte swizzle) into a 2-stage ring.
-//   warp 1      TMEM allocation; one thread issues the MMAs:
-//               S = Q K^T  (M 128 heads, N 32 keys, K 576: 36 x K16, both
-//               operands K-major) and O += P V (M 128, N 256, K 32; P
-//               K-major with 64-byte swizzle, V = the same smem tile read
-//               MN-major).
-//   warps 4..7  softmax, one thread per head: S from TMEM, mask j >= lim,
-//               exp2-domain online softmax with a lazily updated max (O in
-//               TMEM is rescaled only when the max grows by more than 2^8),
-//               P rounded to bf16 into shared memory; epilogue.
+// CTA's output half O[128 x 256] (fp32), two score buffers S[128 x 32] and
+// query dims [0, 384) as bf16 pairs (the A operand of 24 of the 36 K16 steps
+// of S: an MMA with A in TMEM reads only B from shared memory, and shared
+// memory bandwidth is what bounds these N = 32 MMAs).
+//   warp 0      TMA: query dims [384, 576) of the token once (48 KB), then
+//               32-key tiles of the latent cache (9 boxes of 64 dims per
+//               16-token page piece, 128-byte swizzle) into a 4-stage ring
+//               (FP8: e4m3 boxes into a 2-stage ring, converted into a
+//               3-stage bf16 ring by warps 2, 3, 8..11).
+//   warp 1      TMEM allocation; MMA issue (one elected lane, warp-uniform
+//               descriptors): S = Q K^T (M 128 heads, N 32 keys, K 576: 24
+//               K16 steps with A from TMEM, 12 with A from shared memory) and
+//               O += P V (M 128, N 256, K 32; P K-major with 64-byte swizzle,
+//               V = the same smem tile read MN-major).
+//   warps 4..7  query dims [0, 384) into TMEM, then softmax, one thread per
+//               head: S from TMEM, mask j >= lim, exp2-domain online softmax
+//               with a lazily updated max (O in TMEM is rescaled only when
+//               the max grows by more than 2^8), P rounded to bf16 into
+//               shared memory; epilogue.
 // The two halves both compute S (576-wide Q K^T) and each does half of P V.
 // Splits of a request publish fp32 (O half, m, l) partials; the last CTA of a
 // (request, token, half) merges them and resets its arrival counter.
@@ -38,9 +44,11 @@ namespace {
 
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kChunks = kMlaLk / 64;            // 9 64-dim chunks of a latent row
+constexpr int kQtChunks = 6;                    // query dims [0, 384) live in TMEM
+constexpr int kQsChunks = kChunks - kQtChunks;  // dims [384, 576) in shared memory
 constexpr int kQChunkBytes = kMlaHeads * 128;   // 16 KB: 128 rows x 64 dims
 constexpr int kKChunkBytes = kMlaTile * 128;    // 4 KB: 32 keys x 64 dims (bf16)
-constexpr int kQBytes = kChunks * kQChunkBytes;     // 147456
+constexpr int kQsBytes = kQsChunks * kQChunkBytes;  // 49152
 constexpr int kStageBytes = kChunks * kKChunkBytes; // 36864: one bf16 tile
 constexpr int kF8StageBytes = kStageBytes / 2;      // 18432: one e4m3 tile
 constexpr int kF8BoxBytes = 16 * 64;                // 16 keys x 64 dims of e4m3
@@ -52,9 +60,9 @@ constexpr int kPBytes = kMlaHeads * kMlaTile * 2;   // 8192 (64-byte rows)
 template <bool kFp8>
 struct Cfg {
   static constexpr int kThreads = kFp8 ? 384 : 256;  // FP8: warps 2, 3, 8..11 convert
-  static constexpr int kStages = kFp8 ? 1 : 2;
-  static constexpr int kF8Stages = kFp8 ? 2 : 0;
-  static constexpr int kOffStages = kQBytes;
+  static constexpr int kStages = kFp8 ? 3 : 4;        // bf16 tiles the MMAs read
+  static constexpr int kF8Stages = kFp8 ? 2 : 0;      // e4m3 tiles TMA lands
+  static constexpr int kOffStages = kQsBytes;
   static constexpr int kOffF8 = kOffStages + kStages * kStageBytes;
   static constexpr int kOffP = kOffF8 + kF8Stages * kF8StageBytes;
   static constexpr int kOffBars = kOffP + kPBytes;
@@ -67,12 +75,14 @@ struct Cfg {
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;     // columns [0, 256): O half
 constexpr uint32_t kTmemS = 256;   // columns [256, 320): two S buffers of 32
+constexpr uint32_t kTmemQ = 320;   // columns [320, 512): query dims [0, 384), bf16 pairs
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
 
 // barrier indices
-enum { kQFull = 0, kKvFull = 1, kKvEmpty = 3, kSFull = 5, kSFree = 7, kPFull = 9, kPvDone = 10,
-       kF8Full = 11, kF8Empty = 13, kBfFull = 15, kBfFree = 16, kNumBars = 17 };
+enum { kQFull = 0, kQtReady = 1, kKvFull = 2, kKvEmpty = 6, kSFull = 10, kSFree = 12, kPFull = 14,
+       kPvDone = 15, kF8Full = 16, kF8Empty = 20, kNumBars = 24 };
+constexpr int kMaxStages = 4;
 constexpr int kConverters = 192;  // FP8: six converter warps
 
 struct Unit {
@@ -141,22 +151,22 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   int* flag = reinterpret_cast<int*>(base + C::kOffBars + 8 * kNumBars + 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  static_assert(C::kStages <= kMaxStages && C::kF8Stages <= kMaxStages, "barrier slots");
   if (tid == 0) {
     mbar_init(bar(kQFull), 1);
-    for (int s = 0; s < 2; ++s) {  // every barrier either path may touch
+    mbar_init(bar(kQtReady), 128);
+    for (int s = 0; s < kMaxStages; ++s) {  // every barrier either path may touch
       mbar_init(bar(kKvFull + s), 1);
       mbar_init(bar(kKvEmpty + s), 1);
-      mbar_init(bar(kSFull + s), 1);   // two score buffers on both paths
+      mbar_init(bar(kF8Full + s), 1);
+      mbar_init(bar(kF8Empty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kSFull + s), 1);
       mbar_init(bar(kSFree + s), 128);
     }
     mbar_init(bar(kPFull), 1);
     mbar_init(bar(kPvDone), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kF8Full + s), 1);
-      mbar_init(bar(kF8Empty + s), 1);
-    }
-    mbar_init(bar(kBfFull), 1);
-    mbar_init(bar(kBfFree), 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -180,21 +190,28 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     if (n > 0) {
       const int qrow = u.b * p.qlen + u.t;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(kQFull), kQBytes);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_3d(sQ + c * kQChunkBytes, &q_map, bar(kQFull), 64 * c, 0, qrow);
+        mbar_arrive_expect_tx(bar(kQFull), kQsBytes);
+        for (int c = 0; c < kQsChunks; ++c)
+          tma_load_3d(sQ + c * kQChunkBytes, &q_map, bar(kQFull), 64 * (kQtChunks + c), 0, qrow);
       }
       const int32_t* bt_row = p.bt + (long long)u.b * p.bt_sb;
-      for (int g = 0; g < n; g += 16) {
-        // lane l holds the block id of 16-key piece l of tiles [g, g + 16)
-        const int piece_tok = (u.tile0 + g) * kMlaTile + 16 * lane;
-        int blk = p.num_pages;  // out of range: TMA fills zeros
-        int off = 0;
-        if (piece_tok < u.L && lane < 2 * (n - g)) {
+      // lane l holds the block id / page offset of 16-key piece l of the tiles
+      // [gg, gg + 16); out-of-range pieces point past the cache (TMA fills zeros).
+      // (An L2 prefetch of the tiles ahead, 18 more TMA operations per tile,
+      // measured slower: the TMA unit's operation rate, not latency, limits.)
+      auto piece = [&](int gg, int& blk, int& off) {
+        const int piece_tok = (u.tile0 + gg) * kMlaTile + 16 * lane;
+        blk = p.num_pages;
+        off = 0;
+        if (gg < n && piece_tok < u.L && lane < 2 * (n - gg)) {
           blk = __ldg(bt_row + piece_tok / p.page_size);
           off = piece_tok % p.page_size;
           if (blk < 0 || blk >= p.num_pages) atomicOr(p.err, DEVERR_BAD_BLOCK);
         }
+      };
+      for (int g = 0; g < n; g += 16) {
+        int blk, off;
+        piece(g, blk, off);
         for (int i = g; i < min(n, g + 16); ++i) {
           const int b0 = __shfl_sync(0xffffffffu, blk, 2 * (i - g));
           const int o0 = __shfl_sync(0xffffffffu, off, 2 * (i - g));
@@ -213,8 +230,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           } else if (lane == 0) {
             // e4m3 boxes of 16 keys x 64 dims, unswizzled: box (piece h, chunk c)
             // at (h * 9 + c) * 1 KB, 64-byte rows
-            const int st = i & 1;
-            mbar_wait(bar(kF8Empty + st), ((i >> 1) & 1) ^ 1u, p.err);
+            const int st = i % C::kF8Stages;
+            mbar_wait(bar(kF8Empty + st), ((i / C::kF8Stages) & 1) ^ 1u, p.err);
             mbar_arrive_expect_tx(bar(kF8Full + st), kF8StageBytes);
             const uint32_t dst = sF8 + st * kF8StageBytes;
             for (int c = 0; c < kChunks; ++c) {
@@ -228,47 +245,55 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ============================= MMA issuer =============================
-    if (n > 0 && lane == 0) {
+    if (n > 0) {
       const uint32_t id_s = tc::idesc_bf16_f32(128, kMlaTile, false, false);
       const uint32_t id_pv = tc::idesc_bf16_f32(128, kMlaHalf, false, true);
       mbar_wait(bar(kQFull), 0, p.err);
+      mbar_wait(bar(kQtReady), 0, p.err);
       auto do_pv = [&](int j) {
         mbar_wait(bar(kPFull), j & 1, p.err);
         tc::fence_after_sync();
         const uint32_t v0 = sK + (j % kStages) * kStageBytes + (4 * u.half) * kKChunkBytes;
 #pragma unroll
         for (int ks = 0; ks < kMlaTile / 16; ++ks)
-          tc::mma_bf16(tmem + kTmemO, tc::smem_desc(sP + ks * 32, 16, 512, tc::kSwizzle64),
-                       tc::smem_desc(v0 + ks * 2048, kKChunkBytes, 1024, tc::kSwizzle128), id_pv,
-                       j > 0 || ks > 0);
-        tc::commit(bar(kPvDone));
-        tc::commit(bar(kFp8 ? kBfFree : kKvEmpty + j % kStages));
+          tc::mma_bf16_elect(tmem + kTmemO, tc::smem_desc(sP + ks * 32, 16, 512, tc::kSwizzle64),
+                             tc::smem_desc(v0 + ks * 2048, kKChunkBytes, 1024, tc::kSwizzle128),
+                             id_pv, j > 0 || ks > 0);
+        tc::commit_elect(bar(kPvDone));
+        tc::commit_elect(bar(kKvEmpty + j % kStages));
       };
       for (int i = 0; i < n; ++i) {
         const int st = i % kStages, sb = i & 1;
-        if (kFp8)
-          mbar_wait(bar(kBfFull), i & 1, p.err);
-        else
-          mbar_wait(bar(kKvFull + st), (i / kStages) & 1, p.err);
+        mbar_wait(bar(kKvFull + st), (i / kStages) & 1, p.err);
         mbar_wait(bar(kSFree + sb), ((i >> 1) & 1) ^ 1u, p.err);
         tc::fence_after_sync();
         const uint32_t kst = sK + st * kStageBytes;
-        for (int c = 0; c < kChunks; ++c) {
+        const uint32_t d = tmem + kTmemS + sb * kMlaTile;
+        // dims [0, 384): A = query from TMEM (8 columns per K16 step)
+#pragma unroll 1
+        for (int c = 0; c < kQtChunks; ++c) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem + kTmemS + sb * kMlaTile,
-                         tc::smem_desc(sQ + c * kQChunkBytes + ks * 32, 16, 1024, tc::kSwizzle128),
-                         tc::smem_desc(kst + c * kKChunkBytes + ks * 32, 16, 1024, tc::kSwizzle128),
-                         id_s, (c | ks) != 0);
+            tc::mma_bf16_ts_elect(
+                d, tmem + kTmemQ + (4 * c + ks) * 8,
+                tc::smem_desc(kst + c * kKChunkBytes + ks * 32, 16, 1024, tc::kSwizzle128), id_s,
+                (c | ks) != 0);
         }
-        tc::commit(bar(kSFull + sb));
-        if (kFp8) {
-          do_pv(i);  // the single bf16 stage is converted again only after P V
-        } else if (i > 0) {
-          do_pv(i - 1);
+        // dims [384, 576): A = query from shared memory
+#pragma unroll 1
+        for (int c = kQtChunks; c < kChunks; ++c) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_bf16_elect(
+                d, tc::smem_desc(sQ + (c - kQtChunks) * kQChunkBytes + ks * 32, 16, 1024,
+                                 tc::kSwizzle128),
+                tc::smem_desc(kst + c * kKChunkBytes + ks * 32, 16, 1024, tc::kSwizzle128), id_s,
+                true);
         }
+        tc::commit_elect(bar(kSFull + sb));
+        if (i > 0) do_pv(i - 1);
       }
-      if (!kFp8) do_pv(n - 1);
+      do_pv(n - 1);
     }
   } else if (kFp8 && (warp == 2 || warp == 3 || warp >= 8)) {
     // ============ FP8: e4m3 tile -> bf16 tile in the MMA's swizzled layout ============
@@ -276,11 +301,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     // and to the output instead.
     const int ct = (warp < 8) ? tid - 64 : tid - 256 + 64;  // 0 .. 191
     for (int i = 0; i < n; ++i) {
-      const int st = i & 1;
-      mbar_wait(bar(kF8Full + st), (i >> 1) & 1, p.err);
-      if (i > 0) mbar_wait(bar(kBfFree), (i - 1) & 1, p.err);  // P V of tile i-1 is done
-      const uint8_t* src = base + C::kOffF8 + st * kF8StageBytes;
-      uint8_t* dst = base + C::kOffStages;
+      const int sf = i % C::kF8Stages, st = i % kStages;
+      mbar_wait(bar(kF8Full + sf), (i / C::kF8Stages) & 1, p.err);
+      // the bf16 stage is free once P V of its previous tile is done
+      mbar_wait(bar(kKvEmpty + st), ((i / kStages) & 1) ^ 1u, p.err);
+      const uint8_t* src = base + C::kOffF8 + sf * kF8StageBytes;
+      uint8_t* dst = base + C::kOffStages + st * kStageBytes;
       // 1152 items: (piece h, chunk c, key row rr of 16, 16-byte e4m3 unit q of 4)
       for (int it = ct; it < 2 * kChunks * 16 * 4; it += kConverters) {
         const int q = it & 3, rr = (it >> 2) & 15, hc = it >> 6;  // hc = h * 9 + c
@@ -312,8 +338,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       __syncwarp();
       named_bar_sync(2, kConverters);
       if (ct == 0) {
-        mbar_arrive(bar(kF8Empty + st));
-        mbar_arrive(bar(kBfFull));
+        mbar_arrive(bar(kF8Empty + sf));
+        mbar_arrive(bar(kKvFull + st));
       }
     }
   } else if (warp >= kSoftmaxWarp0 && warp < 8) {
@@ -323,6 +349,28 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     float m_used = -INFINITY, l = 0.f;
     uint8_t* p_row = base + C::kOffP + (row / 8) * 512 + (row % 8) * 64;
     const int pswz = (row % 8) >> 1;
+    if (n > 0) {
+      // query dims [0, 384) of this head into TMEM lane `row`: the A operand
+      // of the first 24 K16 steps of S = Q K^T
+      const uint4* qsrc = reinterpret_cast<const uint4*>(
+          p.q + ((long long)u.b * p.qlen + u.t) * p.q_sr + (long long)row * p.q_sh);
+#pragma unroll 1
+      for (int j = 0; j < kQtChunks; ++j) {
+        uint32_t v[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 w = __ldg(qsrc + 8 * j + k);
+          v[4 * k] = w.x;
+          v[4 * k + 1] = w.y;
+          v[4 * k + 2] = w.z;
+          v[4 * k + 3] = w.w;
+        }
+        tc::st_32x32b_x32(tmem + lane_base + kTmemQ + 32 * j, v);
+      }
+      tc::wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(bar(kQtReady));
+    }
     for (int i = 0; i < n; ++i) {
       const int sb = i & 1;
       mbar_wait(bar(kSFull + sb), (i >> 1) & 1, p.err);
@@ -464,39 +512,63 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       named_bar_sync(1, 128);
       if (*flag == u.nsplit - 1) {
         // last split of this (request, token, half): merge every partial
+        // (m, l) of every split first (independent loads), then O in 32-dim
+        // chunks with the loads of several splits in flight
+        const int ns = u.nsplit;
+        float ms_[16], ls_[16];
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+          if (s < ns) {
+            const float* ml =
+                p.partials + slot_of(p, u, s) * kMlaPartialFloats + kMlaHeads * kMlaHalf;
+            ms_[s] = __ldcg(ml + row);
+            ls_[s] = __ldcg(ml + kMlaHeads + row);
+          }
+        }
         float M = -INFINITY;
-        for (int s = 0; s < u.nsplit; ++s)
-          M = fmaxf(M, __ldcg(p.partials + slot_of(p, u, s) * kMlaPartialFloats +
-                              kMlaHeads * kMlaHalf + row));
+#pragma unroll
+        for (int s = 0; s < 16; ++s)
+          if (s < ns) M = fmaxf(M, ms_[s]);
         float Ls = 0.f;
         float w[16];
-        const int ns = u.nsplit;
-        for (int s = 0; s < ns; ++s) {
-          const float* ml = p.partials + slot_of(p, u, s) * kMlaPartialFloats + kMlaHeads * kMlaHalf;
-          const float ms = __ldcg(ml + row);
-          const float ws = (ms == -INFINITY) ? 0.f : ex2((ms - M) * c2);
-          Ls = __fmaf_rn(ws, __ldcg(ml + kMlaHeads + row), Ls);
-          if (s < 16) w[s] = ws;
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+          w[s] = 0.f;
+          if (s < ns) {
+            w[s] = (ms_[s] == -INFINITY) ? 0.f : ex2((ms_[s] - M) * c2);
+            Ls = __fmaf_rn(w[s], ls_[s], Ls);
+          }
         }
         const float inv = (Ls > 0.f) ? out_scale / Ls : 0.f;
-        for (int j = 0; j < kMlaHalf; j += 8) {
-          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < kMlaHalf; j += 32) {
+          float acc[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+#pragma unroll 4
           for (int s = 0; s < ns; ++s) {
-            const float* src = p.partials + slot_of(p, u, s) * kMlaPartialFloats +
-                               (long long)row * kMlaHalf + j;
-            const float4 a = ldcg_f4(src), bq = ldcg_f4(src + 4);
+            const float* src =
+                p.partials + slot_of(p, u, s) * kMlaPartialFloats + (long long)row * kMlaHalf + j;
+            float4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = ldcg_f4(src + 4 * k);
             const float ws = w[s];
-            acc[0] = __fmaf_rn(ws, a.x, acc[0]); acc[1] = __fmaf_rn(ws, a.y, acc[1]);
-            acc[2] = __fmaf_rn(ws, a.z, acc[2]); acc[3] = __fmaf_rn(ws, a.w, acc[3]);
-            acc[4] = __fmaf_rn(ws, bq.x, acc[4]); acc[5] = __fmaf_rn(ws, bq.y, acc[5]);
-            acc[6] = __fmaf_rn(ws, bq.z, acc[6]); acc[7] = __fmaf_rn(ws, bq.w, acc[7]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              acc[4 * k] = __fmaf_rn(ws, v[k].x, acc[4 * k]);
+              acc[4 * k + 1] = __fmaf_rn(ws, v[k].y, acc[4 * k + 1]);
+              acc[4 * k + 2] = __fmaf_rn(ws, v[k].z, acc[4 * k + 2]);
+              acc[4 * k + 3] = __fmaf_rn(ws, v[k].w, acc[4 * k + 3]);
+            }
           }
-          uint4 v;
-          v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-          v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-          v.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-          v.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-          *reinterpret_cast<uint4*>(out_row + j) = v;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 v;
+            v.x = pack_bf16(acc[8 * k] * inv, acc[8 * k + 1] * inv);
+            v.y = pack_bf16(acc[8 * k + 2] * inv, acc[8 * k + 3] * inv);
+            v.z = pack_bf16(acc[8 * k + 4] * inv, acc[8 * k + 5] * inv);
+            v.w = pack_bf16(acc[8 * k + 6] * inv, acc[8 * k + 7] * inv);
+            *reinterpret_cast<uint4*>(out_row + j + 8 * k) = v;
+          }
         }
         if (u.half == 0)
           p.lse[r * p.lse_sr + row * p.lse_sh] = (Ls > 0.f) ? M * scale_eff + logf(Ls) : -INFINITY;

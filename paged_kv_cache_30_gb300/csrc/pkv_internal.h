@@ -97,10 +97,14 @@ constexpr int kMlaLk = 576;
 constexpr int kMlaLv = 512;
 constexpr int kMlaHalf = kMlaLv / 2;        // output dims per CTA
 constexpr int kMlaTile = 32;                // keys per pipeline tile
-constexpr int kMlaMinTiles = 32;            // a split holds at least 1024 keys
+constexpr int kMlaMinTiles = 128;           // a split holds at least 4096 keys
 constexpr int64_t kMlaPartialFloats = int64_t(kMlaHeads) * kMlaHalf + 2 * kMlaHeads;
 
 struct MlaParams {
+  const uint16_t* q;             // bf16 [B*qlen, 128, 576]
+  int64_t q_sr, q_sh;
+  const uint8_t* kv;             // latent cache base
+  int64_t kv_stok, kv_spage;     // token / page strides in bytes
   const int32_t* bt;
   int64_t bt_sb;
   int max_blocks;
