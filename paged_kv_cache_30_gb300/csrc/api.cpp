@@ -567,13 +567,16 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
     if (cr != CUDA_SUCCESS) return fail(PKV_ERR_INVALID_ARG, "q tensor map rejected (%d)", (int)cr);
   }
   {
-    const cuuint64_t gdim[3] = {cuuint64_t(Lk), cuuint64_t(page_size), cuuint64_t(num_pages)};
-    const cuuint64_t gstr[2] = {cuuint64_t(s_tok) * esz, cuuint64_t(s_page) * esz};
-    const cuuint32_t box[3] = {64, 16, 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    // bf16: 128-byte rows swizzled for the MMA; e4m3: 64-byte rows, plain (converted in smem)
+    // the cache viewed as (64 dims, tokens, 9 chunks of 64 dims, pages): a box
+    // of (64, n tokens, 9, 1) lands chunk-major, n rows of 128 (bf16, 128-byte
+    // swizzle) or 64 (e4m3, plain) bytes per chunk
+    const cuuint64_t gdim[4] = {64, cuuint64_t(page_size), 9, cuuint64_t(num_pages)};
+    const cuuint64_t gstr[3] = {cuuint64_t(s_tok) * esz, cuuint64_t(64 * esz),
+                                cuuint64_t(s_page) * esz};
+    const cuuint32_t box[4] = {64, fp8 ? 16u : 8u, 9, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult cr = encode(&kv_map,
-                         fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                         fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                          latent_cache->data, gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -16,10 +16,15 @@
 // of S: an MMA with A in TMEM reads only B from shared memory, and shared
 // memory bandwidth is what bounds these N = 32 MMAs).
 //   warp 0      TMA: query dims [384, 576) of the token once (48 KB), then
-//               32-key tiles of the latent cache (9 boxes of 64 dims per
-//               16-token page piece, 128-byte swizzle) into a 4-stage ring
-//               (FP8: e4m3 boxes into a 2-stage ring, converted into a
-//               3-stage bf16 ring by warps 2, 3, 8..11).
+//               32-key tiles of the latent cache into a 4-stage ring (FP8:
+//               e4m3 into a 2-stage ring, converted into a 3-stage bf16 ring
+//               by warps 2, 3, 8..11).  The cache is read as a 4-D tensor
+//               (64 dims, token, 9 chunks of 64 dims, page): one box of 8
+//               tokens x 9 chunks (16 for e4m3) lands chunk-major, so a tile
+//               is 4 groups of 8 keys, 9216 bytes apart, and chunk c of group
+//               g is one 1024-byte 128-byte-swizzle atom at g * 9216 + c * 1024
+//               -- both the K-major S operand and the MN-major V operand are
+//               plain descriptors over it (stride 9216 between 8-key groups).
 //   warp 1      TMEM allocation; MMA issue (one elected lane, warp-uniform
 //               descriptors): S = Q K^T (M 128 heads, N 32 keys, K 576: 24
 //               K16 steps with A from TMEM, 12 with A from shared memory) and
@@ -47,16 +52,16 @@ constexpr int kChunks = kMlaLk / 64;            // 9 64-dim chunks of a latent r
 constexpr int kQtChunks = 6;                    // query dims [0, 384) live in TMEM
 constexpr int kQsChunks = kChunks - kQtChunks;  // dims [384, 576) in shared memory
 constexpr int kQChunkBytes = kMlaHeads * 128;   // 16 KB: 128 rows x 64 dims
-constexpr int kKChunkBytes = kMlaTile * 128;    // 4 KB: 32 keys x 64 dims (bf16)
 constexpr int kQsBytes = kQsChunks * kQChunkBytes;  // 49152
-constexpr int kStageBytes = kChunks * kKChunkBytes; // 36864: one bf16 tile
+constexpr int kGroupBytes = kChunks * 1024;     // 9216: 8 keys x 576 dims, chunk-major
+constexpr int kStageBytes = kMlaTile / 8 * kGroupBytes;  // 36864: one bf16 tile
 constexpr int kF8StageBytes = kStageBytes / 2;      // 18432: one e4m3 tile
-constexpr int kF8BoxBytes = 16 * 64;                // 16 keys x 64 dims of e4m3
 constexpr int kPBytes = kMlaHeads * kMlaTile * 2;   // 8192 (64-byte rows)
 
-// Shared memory: [Q | bf16 tile stages | e4m3 tile stages (FP8 only) | P | barriers].
-// The bf16 path double-buffers its bf16 tiles; the FP8 path double-buffers the
-// e4m3 tiles that TMA lands and converts each into a single bf16 stage.
+// Shared memory: [query dims 384..575 | bf16 tile stages | e4m3 tile stages
+// (FP8 only) | P | barriers].  The bf16 path keeps 4 tiles in flight; the FP8
+// path lands e4m3 tiles in a 2-stage ring and converts each into one of 3
+// bf16 stages.
 template <bool kFp8>
 struct Cfg {
   static constexpr int kThreads = kFp8 ? 384 : 256;  // FP8: warps 2, 3, 8..11 convert
@@ -222,11 +227,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             mbar_wait(bar(kKvEmpty + st), ((i / kStages) & 1) ^ 1u, p.err);
             mbar_arrive_expect_tx(bar(kKvFull + st), kStageBytes);
             const uint32_t dst = sK + st * kStageBytes;
-            for (int c = 0; c < kChunks; ++c) {
-              tma_load_3d(dst + c * kKChunkBytes, &kv_map, bar(kKvFull + st), 64 * c, o0, b0);
-              tma_load_3d(dst + c * kKChunkBytes + 2048, &kv_map, bar(kKvFull + st), 64 * c, o1,
-                          b1);
-            }
+            // four boxes of 8 keys x 9 chunks: group g at g * 9216, chunk c of it
+            // at + c * 1024 (one 128-byte-swizzle atom)
+            tma_load_4d(dst, &kv_map, bar(kKvFull + st), 0, o0, 0, b0);
+            tma_load_4d(dst + kGroupBytes, &kv_map, bar(kKvFull + st), 0, o0 + 8, 0, b0);
+            tma_load_4d(dst + 2 * kGroupBytes, &kv_map, bar(kKvFull + st), 0, o1, 0, b1);
+            tma_load_4d(dst + 3 * kGroupBytes, &kv_map, bar(kKvFull + st), 0, o1 + 8, 0, b1);
           } else if (lane == 0) {
             // e4m3 boxes of 16 keys x 64 dims, unswizzled: box (piece h, chunk c)
             // at (h * 9 + c) * 1 KB, 64-byte rows
@@ -234,11 +240,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             mbar_wait(bar(kF8Empty + st), ((i / C::kF8Stages) & 1) ^ 1u, p.err);
             mbar_arrive_expect_tx(bar(kF8Full + st), kF8StageBytes);
             const uint32_t dst = sF8 + st * kF8StageBytes;
-            for (int c = 0; c < kChunks; ++c) {
-              tma_load_3d(dst + c * kF8BoxBytes, &kv_map, bar(kF8Full + st), 64 * c, o0, b0);
-              tma_load_3d(dst + (kChunks + c) * kF8BoxBytes, &kv_map, bar(kF8Full + st), 64 * c,
-                          o1, b1);
-            }
+            // two boxes of 16 keys x 9 chunks: piece h at h * 9216, chunk c of it
+            // at + c * 1024, 64-byte rows
+            tma_load_4d(dst, &kv_map, bar(kF8Full + st), 0, o0, 0, b0);
+            tma_load_4d(dst + kGroupBytes, &kv_map, bar(kF8Full + st), 0, o1, 0, b1);
           }
         }
       }
@@ -253,11 +258,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       auto do_pv = [&](int j) {
         mbar_wait(bar(kPFull), j & 1, p.err);
         tc::fence_after_sync();
-        const uint32_t v0 = sK + (j % kStages) * kStageBytes + (4 * u.half) * kKChunkBytes;
+        const uint32_t v0 = sK + (j % kStages) * kStageBytes + (4 * u.half) * 1024;
 #pragma unroll
         for (int ks = 0; ks < kMlaTile / 16; ++ks)
           tc::mma_bf16_elect(tmem + kTmemO, tc::smem_desc(sP + ks * 32, 16, 512, tc::kSwizzle64),
-                             tc::smem_desc(v0 + ks * 2048, kKChunkBytes, 1024, tc::kSwizzle128),
+                             tc::smem_desc(v0 + ks * 2 * kGroupBytes, 1024, kGroupBytes,
+                                           tc::kSwizzle128),
                              id_pv, j > 0 || ks > 0);
         tc::commit_elect(bar(kPvDone));
         tc::commit_elect(bar(kKvEmpty + j % kStages));
@@ -276,7 +282,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           for (int ks = 0; ks < 4; ++ks)
             tc::mma_bf16_ts_elect(
                 d, tmem + kTmemQ + (4 * c + ks) * 8,
-                tc::smem_desc(kst + c * kKChunkBytes + ks * 32, 16, 1024, tc::kSwizzle128), id_s,
+                tc::smem_desc(kst + c * 1024 + ks * 32, 16, kGroupBytes, tc::kSwizzle128), id_s,
                 (c | ks) != 0);
         }
         // dims [384, 576): A = query from shared memory
@@ -287,7 +293,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
             tc::mma_bf16_elect(
                 d, tc::smem_desc(sQ + (c - kQtChunks) * kQChunkBytes + ks * 32, 16, 1024,
                                  tc::kSwizzle128),
-                tc::smem_desc(kst + c * kKChunkBytes + ks * 32, 16, 1024, tc::kSwizzle128), id_s,
+                tc::smem_desc(kst + c * 1024 + ks * 32, 16, kGroupBytes, tc::kSwizzle128), id_s,
                 true);
         }
         tc::commit_elect(bar(kSFull + sb));
@@ -311,7 +317,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       for (int it = ct; it < 2 * kChunks * 16 * 4; it += kConverters) {
         const int q = it & 3, rr = (it >> 2) & 15, hc = it >> 6;  // hc = h * 9 + c
         const int h = hc / kChunks, c = hc % kChunks;
-        const uint4 w = *reinterpret_cast<const uint4*>(src + hc * kF8BoxBytes + rr * 64 + q * 16);
+        const uint4 w =
+            *reinterpret_cast<const uint4*>(src + h * kGroupBytes + c * 1024 + rr * 64 + q * 16);
         const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
         uint32_t o[8];
 #pragma unroll
@@ -327,7 +334,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           }
         }
         const int row = 16 * h + rr;  // key row of the tile
-        uint8_t* rowp = dst + c * kKChunkBytes + (row / 8) * 1024 + (row % 8) * 128;
+        uint8_t* rowp = dst + (row / 8) * kGroupBytes + c * 1024 + (row % 8) * 128;
         // e4m3 unit q holds dims 16q .. 16q + 15 = bf16 units 2q, 2q + 1
         *reinterpret_cast<uint4*>(rowp + (((2 * q) ^ (row % 8)) * 16)) =
             make_uint4(o[0], o[1], o[2], o[3]);
@@ -441,11 +448,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         // keys past the row limit: zero their V rows (this CTA's 256 dims) so
         // stale or poisoned cache contents never meet P = 0 in the MMA
         uint8_t* vst =
-            base + C::kOffStages + (i % kStages) * kStageBytes + 4 * u.half * kKChunkBytes;
+            base + C::kOffStages + (i % kStages) * kStageBytes + 4 * u.half * 1024;
         const int nz = kMlaTile - max(nvalid, 0);
         for (int q = row; q < nz * 4 * 8; q += 128) {
           const int rr = max(nvalid, 0) + q / 32, ch = (q / 8) % 4, un = q % 8;
-          *reinterpret_cast<uint4*>(vst + ch * kKChunkBytes + (rr / 8) * 1024 + (rr % 8) * 128 +
+          *reinterpret_cast<uint4*>(vst + (rr / 8) * kGroupBytes + ch * 1024 + (rr % 8) * 128 +
                                     un * 16) = make_uint4(0, 0, 0, 0);
         }
       }
