@@ -173,6 +173,29 @@ int get_encoder(EncodeTiledFn* fn) {
   return PKV_OK;
 }
 
+// The GQA cache [blocks, Hkv, P, 256] viewed as (64 dims, token, 4 chunks of 64
+// dims, kv head, block): a box of (64, 16, 4, 1, 1) is one 16-token tile of one
+// kv head, landing chunk-major (K lo, K hi, V lo, V hi; 16 rows of 128 bytes
+// each, 128-byte swizzle) -- one TMA operation per 8 KB tile.
+int encode_gqa_kv_map(EncodeTiledFn encode, const pkv_tensor* kv_cache, int page_size,
+                      CUtensorMap* map) {
+  const cuuint64_t gdim[5] = {64, cuuint64_t(page_size), 4, cuuint64_t(kv_cache->shape[1]),
+                              cuuint64_t(kv_cache->shape[0])};
+  const cuuint64_t gstride[4] = {cuuint64_t(kv_cache->stride[2]) * 2, 128,
+                                 cuuint64_t(kv_cache->stride[1]) * 2,
+                                 cuuint64_t(kv_cache->stride[0]) * 2};
+  const cuuint32_t box[5] = {64, 16, 4, 1, 1};
+  const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+  const CUresult cr = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, kv_cache->data, gdim,
+                             gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS)
+    return fail(PKV_ERR_INVALID_ARG, "cuTensorMapEncodeTiled rejected the kv_cache layout (%d)",
+                (int)cr);
+  return PKV_OK;
+}
+
 }  // namespace
 
 // =================================================================== ABI ==
@@ -402,19 +425,7 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
   EncodeTiledFn encode = nullptr;
   if ((rc = get_encoder(&encode))) return rc;
   CUtensorMap map;
-  const cuuint64_t gdim[4] = {cuuint64_t(2 * D), cuuint64_t(page_size), cuuint64_t(Hkv),
-                              cuuint64_t(nb)};
-  const cuuint64_t gstride[3] = {cuuint64_t(kv_cache->stride[2]) * 2,
-                                 cuuint64_t(kv_cache->stride[1]) * 2,
-                                 cuuint64_t(kv_cache->stride[0]) * 2};
-  const cuuint32_t box[4] = {64, 16, 1, 1};  // one 64-wide slice of a 16-token tile
-  const cuuint32_t estride[4] = {1, 1, 1, 1};
-  CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, kv_cache->data, gdim, gstride,
-                       box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS)
-    return fail(PKV_ERR_INVALID_ARG, "cuTensorMapEncodeTiled rejected the kv_cache layout (%d)",
-                (int)cr);
+  if ((rc = encode_gqa_kv_map(encode, kv_cache, page_size, &map))) return rc;
 
   pkv::GqaParams p;
   std::memset(&p, 0, sizeof p);
@@ -530,7 +541,7 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
     return fail(PKV_ERR_INVALID_ARG, "q and out last dims must be contiguous");
   if (q->stride[0] % 8 || q->stride[1] % 8 || out->stride[0] % 8 || out->stride[1] % 8 ||
       !aligned16(q->data) || !aligned16(out->data))
-    return fail(PKV_ERR_ALIGNMENT, "q and out must be 16-byte aligned with strides % 8 == 0");
+    return fail(PKV_ERR_ALIGNMENT, "q and out must be 16-byte aligned with strides %% 8 == 0");
   if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
   if (num_kv_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_splits < 0");
   if (B == 0) return PKV_OK;
@@ -696,20 +707,7 @@ int prepare_gqa_call(const pkv_tensor* q, const pkv_tensor* kv_cache,
 
   EncodeTiledFn encode = nullptr;
   if ((rc = get_encoder(&encode))) return rc;
-  const cuuint64_t gdim[4] = {cuuint64_t(2 * D), cuuint64_t(page_size), cuuint64_t(Hkv),
-                              cuuint64_t(nb)};
-  const cuuint64_t gstride[3] = {cuuint64_t(kv_cache->stride[2]) * 2,
-                                 cuuint64_t(kv_cache->stride[1]) * 2,
-                                 cuuint64_t(kv_cache->stride[0]) * 2};
-  const cuuint32_t box[4] = {64, 16, 1, 1};
-  const cuuint32_t estride[4] = {1, 1, 1, 1};
-  const CUresult cr = encode(&call->map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, kv_cache->data,
-                             gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS)
-    return fail(PKV_ERR_INVALID_ARG, "cuTensorMapEncodeTiled rejected the kv_cache layout (%d)",
-                (int)cr);
+  if ((rc = encode_gqa_kv_map(encode, kv_cache, page_size, &call->map))) return rc;
   GqaParams& p = call->p;
   p.q = static_cast<const uint16_t*>(q->data);
   p.q_sb = q->stride[0];

@@ -18,8 +18,10 @@
 //    launch shape depends only on the device and the batch.
 //  * The producer warp bulk-copies the item's 8 query rows into a descriptor
 //    slot, reads block-table entries 32 at a time and streams every 16-token
-//    tile of every page as four 64-element TMA boxes (K lo, K hi, V lo, V hi)
-//    with 128-byte swizzle into an 8-stage ring (8 KB stages) guarded by
+//    tile of every page with one TMA operation -- a 5-D view of the cache
+//    (64 dims, token, 4 chunks of 64 dims, kv head, block) whose box lands the
+//    tile chunk-major as four 16 x 128-byte slabs (K lo, K hi, V lo, V hi) with
+//    128-byte swizzle -- into an 8-stage ring (8 KB stages) guarded by
 //    full/empty mbarriers.  It runs ahead across item boundaries.
 //  * Consumer warp w takes tiles w, w+4, ... of the item.  It pulls the tile's
 //    K and V fragments into registers with ldmatrix (conflict-free thanks to
@@ -321,10 +323,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               mbar_wait(empty_bar(stage), ((seq / kStages) & 1) ^ 1u, p.err);
               mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
               const uint32_t dst = ring + stage * kStageBytes;
-#pragma unroll
-              for (int c = 0; c < 4; ++c)
-                tma_load_4d(dst + c * kBoxBytes, &kv_map, full_bar(stage), 64 * c, 16 * sub, kvh,
-                            blk_i);
+              // one box: 16 tokens x 4 chunks of 64 dims (K lo, K hi, V lo, V hi),
+              // landing chunk-major
+              tma_load_5d(dst, &kv_map, full_bar(stage), 0, 16 * sub, 0, kvh, blk_i);
             }
             ++seq;
           }

@@ -67,6 +67,7 @@ struct Cfg {
   static constexpr int kThreads = kFp8 ? 384 : 256;  // FP8: warps 2, 3, 8..11 convert
   static constexpr int kStages = kFp8 ? 3 : 4;        // bf16 tiles the MMAs read
   static constexpr int kF8Stages = kFp8 ? 2 : 0;      // e4m3 tiles TMA lands
+  static constexpr int kF8Ring = kFp8 ? kF8Stages : 1;  // ring modulus (1 when unused)
   static constexpr int kOffStages = kQsBytes;
   static constexpr int kOffF8 = kOffStages + kStages * kStageBytes;
   static constexpr int kOffP = kOffF8 + kF8Stages * kF8StageBytes;
@@ -236,8 +237,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           } else if (lane == 0) {
             // e4m3 boxes of 16 keys x 64 dims, unswizzled: box (piece h, chunk c)
             // at (h * 9 + c) * 1 KB, 64-byte rows
-            const int st = i % C::kF8Stages;
-            mbar_wait(bar(kF8Empty + st), ((i / C::kF8Stages) & 1) ^ 1u, p.err);
+            const int st = i % C::kF8Ring;
+            mbar_wait(bar(kF8Empty + st), ((i / C::kF8Ring) & 1) ^ 1u, p.err);
             mbar_arrive_expect_tx(bar(kF8Full + st), kF8StageBytes);
             const uint32_t dst = sF8 + st * kF8StageBytes;
             // two boxes of 16 keys x 9 chunks: piece h at h * 9216, chunk c of it
@@ -307,8 +308,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     // and to the output instead.
     const int ct = (warp < 8) ? tid - 64 : tid - 256 + 64;  // 0 .. 191
     for (int i = 0; i < n; ++i) {
-      const int sf = i % C::kF8Stages, st = i % kStages;
-      mbar_wait(bar(kF8Full + sf), (i / C::kF8Stages) & 1, p.err);
+      const int sf = i % C::kF8Ring, st = i % kStages;
+      mbar_wait(bar(kF8Full + sf), (i / C::kF8Ring) & 1, p.err);
       // the bf16 stage is free once P V of its previous tile is done
       mbar_wait(bar(kKvEmpty + st), ((i / kStages) & 1) ^ 1u, p.err);
       const uint8_t* src = base + C::kOffF8 + sf * kF8StageBytes;
