@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import struct
 import threading
 
 __all__ = [
@@ -52,6 +53,9 @@ class PkvError(RuntimeError):
 class PkvTensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
                 ("shape", ctypes.c_int64 * 5), ("stride", ctypes.c_int64 * 5)]
+
+
+assert ctypes.sizeof(PkvTensor) == 96
 
 
 _lock = threading.Lock()
@@ -104,28 +108,35 @@ def _check(rc: int) -> int:
     return rc
 
 
+_DTYPES = None
+
+
 def _dtype_code(t) -> int:
-    import torch
-    m = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.int32: DTYPE_I32,
-         torch.float8_e4m3fn: DTYPE_FP8}
-    if t.dtype not in m:
+    global _DTYPES
+    if _DTYPES is None:
+        import torch
+        _DTYPES = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32, torch.int32: DTYPE_I32,
+                   torch.float8_e4m3fn: DTYPE_FP8}
+    code = _DTYPES.get(t.dtype)
+    if code is None:
         raise PkvError(-1, f"unsupported tensor dtype {t.dtype}")
-    return m[t.dtype]
+    return code
+
+
+_PACK = struct.Struct("<Qii5q5q")  # the byte layout of pkv_tensor (96 bytes)
+_PAD = tuple((0,) * k for k in range(6))
 
 
 def _desc(t):
-    """pkv_tensor for a torch tensor (None -> NULL)."""
+    """pkv_tensor for a torch tensor (None -> NULL), packed in one call."""
     if t is None:
         return None
-    d = PkvTensor()
-    d.data = t.data_ptr()
-    d.dtype = _dtype_code(t)
-    d.ndim = t.dim()
-    if t.dim() > 5:
+    n = t.dim()
+    if n > 5:
         raise PkvError(-1, "tensors of more than 5 dims are not supported")
-    for i in range(t.dim()):
-        d.shape[i] = t.shape[i]
-        d.stride[i] = t.stride(i)
+    pad = _PAD[5 - n]
+    d = PkvTensor.from_buffer_copy(
+        _PACK.pack(t.data_ptr(), _dtype_code(t), n, *t.shape, *pad, *t.stride(), *pad))
     return ctypes.byref(d)
 
 

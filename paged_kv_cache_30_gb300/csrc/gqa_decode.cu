@@ -217,6 +217,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     fence_barrier_init();
   }
   if (warp == kConsumerWarps && lane == 0) tma_prefetch_desc(&kv_map);
+  // Programmatic dependent launch: the setup above touches only shared memory
+  // and the kernel parameters; the inputs and the workspace are read after the
+  // grids this launch depends on (e.g. the previous call) have completed.
+  griddep_wait();
 
   // ---- prologue: the item list, identical in every CTA -------------------
   const int B = p.B;
@@ -273,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       __syncwarp();
       if (item >= total_items) {
         if (lane == 0) {
+          griddep_launch_dependents();  // the queue is empty: this CTA only drains now
           items[slot].item = -1;
           mbar_arrive(ifull_bar(slot));
         }
@@ -557,8 +562,19 @@ cudaError_t launch_page(const GqaParams& p, const CUtensorMap& kv_map, int grid,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  gqa_decode_kernel<P><<<grid, kThreads, kSmemBytes, stream>>>(p, kv_map);
-  return cudaGetLastError();
+  // launched as a programmatic dependent of the previous kernel on the stream:
+  // its launch and shared-memory setup overlap that kernel's tail
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gqa_decode_kernel<P>, p, kv_map);
 }
 
 }  // namespace

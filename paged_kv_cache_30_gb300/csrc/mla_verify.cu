@@ -141,6 +141,11 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
                       const __grid_constant__ CUtensorMap kv_map) {
   using C = Cfg<kFp8>;
   constexpr int kStages = C::kStages;
+  // Programmatic dependent launch: nothing is read before the grids this
+  // launch depends on have completed; the next grid may be scheduled as soon
+  // as every CTA of this one has started (it waits for this grid the same way).
+  griddep_wait();
+  griddep_launch_dependents();
   const Unit u = decode_unit(p);
   if (u.split >= u.nsplit) return;  // this request needs fewer splits
 
@@ -604,9 +609,17 @@ cudaError_t launch_t(const MlaParams& p, const CUtensorMap& q_map, const CUtenso
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  mla_verify_kernel<kFp8><<<grid, Cfg<kFp8>::kThreads, Cfg<kFp8>::kSmemBytes, stream>>>(p, q_map,
-                                                                                       kv_map);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(Cfg<kFp8>::kThreads);
+  cfg.dynamicSmemBytes = Cfg<kFp8>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_verify_kernel<kFp8>, p, q_map, kv_map);
 }
 
 }  // namespace

@@ -65,6 +65,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
   return true;
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// Wait until the grids this launch depends on have completed and their memory
+// is visible (returns at once for an ordinary launch).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the next grid on the stream (if launched as a programmatic dependent) be
+// scheduled once every CTA of this grid has signalled or exited.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 // -------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
