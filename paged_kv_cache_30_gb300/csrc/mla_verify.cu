@@ -97,7 +97,36 @@ struct Unit {
   int tile0, ntiles;  // tiles [tile0, tile0 + ntiles) of this CTA
 };
 
-__device__ __forceinline__ Unit decode_unit(const MlaParams& p) {
+__device__ __forceinline__ int clamped_len(const MlaParams& p, int b) {
+  int L = __ldg(p.seq_lens + b);
+  if (L < 0) L = 0;
+  if ((long long)L > (long long)p.max_blocks * p.page_size) L = p.max_blocks * p.page_size;
+  return L;
+}
+
+// Requests are served longest first: CTA block x belongs to the request of
+// rank x / (cap * qlen * 2) in order of decreasing length (ties by index), so
+// the short requests' CTAs fill the end of the launch.  Every CTA ranks the
+// requests itself (B <= 512; beyond that, request order).
+constexpr int kLptMaxB = 512;
+__device__ __forceinline__ int request_of_rank(const MlaParams& p, int R, int* s_b) {
+  if (p.B > kLptMaxB) return R;
+  if (threadIdx.x == 0) *s_b = R;
+  __syncthreads();
+  for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+    const int Lb = clamped_len(p, b);
+    int r = 0;
+    for (int b2 = 0; b2 < p.B; ++b2) {
+      const int L2 = clamped_len(p, b2);
+      r += (L2 > Lb) || (L2 == Lb && b2 < b);
+    }
+    if (r == R) *s_b = b;
+  }
+  __syncthreads();
+  return *s_b;
+}
+
+__device__ __forceinline__ Unit decode_unit(const MlaParams& p, int* s_b) {
   Unit u;
   int x = blockIdx.x;
   u.half = x & 1;
@@ -105,7 +134,7 @@ __device__ __forceinline__ Unit decode_unit(const MlaParams& p) {
   u.t = x % p.qlen;
   x /= p.qlen;
   u.split = x % p.cap;
-  u.b = x / p.cap;
+  u.b = request_of_rank(p, x / p.cap, s_b);
   int L = __ldg(p.seq_lens + u.b);
   if (L < 0) L = 0;
   if ((long long)L > (long long)p.max_blocks * p.page_size) L = p.max_blocks * p.page_size;
@@ -146,7 +175,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   // as every CTA of this one has started (it waits for this grid the same way).
   griddep_wait();
   griddep_launch_dependents();
-  const Unit u = decode_unit(p);
+  __shared__ int s_rank_b;
+  const Unit u = decode_unit(p, &s_rank_b);
   if (u.split >= u.nsplit) return;  // this request needs fewer splits
 
   extern __shared__ uint8_t smem_raw[];
