@@ -169,3 +169,14 @@ def test_mla_fp8_b128_full_size_sampled_rows():
     prob = W.mla_fp8(0)
     rows = np.random.default_rng(2).choice(128 * 128, size=1024, replace=False)
     check(prob, rows=rows, what="mla fp8 b128")
+
+
+def test_mla_request_order_paths():
+    """Longest-first scheduling: 300 requests with many equal lengths (ranks
+    broken by request index) and 520 requests (beyond the ranking limit, plain
+    request order) -- every row against the oracle."""
+    rng = np.random.default_rng(14)
+    for B, seed in ((300, 14), (520, 15)):
+        L = rng.choice([1, 17, 33, 40], size=B).astype(np.int32)
+        prob = mla_case(seed, L, 1, 16, has_real=False, cap=2)
+        check(prob, what=f"mla order B={B}")
