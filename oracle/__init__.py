@@ -72,6 +72,13 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         i32, i32, i32, i32,      # B, H, Lk, Lv
         vp, i64, vp, vp, i32]    # rows, nrows, out, lse, nthreads
     lib.pkv_oracle_mla_verify.restype = i32
+    lib.pkv_oracle_f32_to_e4m3.restype = ctypes.c_uint8
+    lib.pkv_oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+    i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    lib.pkv_oracle_gqa_kv_append.argtypes = [vp, vp, i64, i64, vp, i64, i64, i64, i64, vp, i64,
+                                             i64, vp, ci, i64, i64, i64, ctypes.POINTER(i64)]
+    lib.pkv_oracle_mla_kv_append.argtypes = [vp, i64, vp, ci, i64, i64, i64, vp, i64, i64, vp, ci,
+                                             ci, ctypes.c_float, i64, i64, ctypes.POINTER(i64)]
     return lib
 
 
@@ -198,3 +205,54 @@ def mla_verify(q, latent_cache, block_table, seq_lens, real_seq_lens, qlen, scal
     if rc != 0:
         raise OracleError(f"pkv_oracle_mla_verify failed with status {rc}")
     return out, lse
+
+
+def f32_to_e4m3(x: float, lib=None) -> int:
+    """e4m3 'fn' code of an fp32 value: nearest, ties to even, saturating at 448."""
+    return (lib or load()).pkv_oracle_f32_to_e4m3(float(np.float32(x)))
+
+
+def gqa_kv_append(k, v, kv_cache, block_table, seq_lens, page_size, lib=None):
+    """Write each request's current token (position seq_lens[b] - 1) into a
+    copy of the GQA cache.  k, v: [B, Hkv, D] bf16; kv_cache: [num_blocks, Hkv,
+    P, 2D] bf16.  Returns (new cache as uint16 numpy array, rows skipped)."""
+    lib = lib or load()
+    kn, vn = _np(k, np.uint16), _np(v, np.uint16)
+    cache = _np(kv_cache, np.uint16).copy()
+    btn, sln = _np(block_table, np.int32), _np(seq_lens, np.int32)
+    B, Hkv, D = kn.shape
+    nb, Hkv2, P, D2 = cache.shape
+    assert Hkv2 == Hkv and D2 == 2 * D and P == page_size
+    skipped = ctypes.c_int64(0)
+    rc = lib.pkv_oracle_gqa_kv_append(_ptr(kn), _ptr(vn), Hkv * D, D, _ptr(cache), Hkv * P * D2,
+                                      P * D2, D2, nb, _ptr(btn), btn.shape[1], btn.shape[1],
+                                      _ptr(sln), int(page_size), B, Hkv, D, ctypes.byref(skipped))
+    if rc != 0:
+        raise OracleError(f"pkv_oracle_gqa_kv_append failed with status {rc}")
+    return cache, skipped.value
+
+
+def mla_kv_append(latent, latent_cache, block_table, seq_lens, qlen, page_size, k_scale=None,
+                  lib=None):
+    """Write verify row t of request b (position seq_lens[b] - qlen + t) into a
+    copy of the latent cache.  latent: [B*qlen, Lk] bf16; latent_cache:
+    [num_pages, P, 1, Lk] bf16 or float8_e4m3fn.  Returns (new cache as a
+    uint16 / uint8 numpy array, rows skipped)."""
+    import torch
+    lib = lib or load()
+    fp8 = int(latent_cache.dtype == torch.float8_e4m3fn)
+    ln = _np(latent, np.uint16)
+    cache = _np(latent_cache, np.uint8 if fp8 else np.uint16).copy()
+    btn, sln = _np(block_table, np.int32), _np(seq_lens, np.int32)
+    R, Lk = ln.shape
+    assert R % qlen == 0
+    num_pages, P, one, Lk2 = cache.shape
+    assert one == 1 and Lk2 == Lk and P == page_size
+    ks = 1.0 if (k_scale is None or not fp8) else float(np.float32(k_scale))
+    skipped = ctypes.c_int64(0)
+    rc = lib.pkv_oracle_mla_kv_append(_ptr(ln), Lk, _ptr(cache), fp8, P * Lk, Lk, num_pages,
+                                      _ptr(btn), btn.shape[1], btn.shape[1], _ptr(sln), int(qlen),
+                                      int(page_size), ks, R // qlen, Lk, ctypes.byref(skipped))
+    if rc != 0:
+        raise OracleError(f"pkv_oracle_mla_kv_append failed with status {rc}")
+    return cache, skipped.value

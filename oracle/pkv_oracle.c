@@ -341,3 +341,135 @@ int pkv_oracle_mla_verify(const uint16_t *q, int64_t q_sr, int64_t q_sh,
                  page_size, B, H, Lk, Lv, rows, nrows, out, lse, ORACLE_OK};
     return run_pool(&a, 1, nthreads);
 }
+
+/* ------------------------------------------------------------------------- */
+/* Paged KV append.
+ *
+ * "Atencion paginada" (transformers), decode path, "Comportamiento de la
+ * cache" and "Ejemplo": the decode kernel updates the paged cache in place;
+ * the new token of a request with cache_seqlens[b] cached tokens goes to
+ * logical position cache_seqlens[b], i.e. page block_table[b][pos / page],
+ * slot pos % page (the example: 30 cached tokens -> block 2 slot 30; 32 ->
+ * the second block, slot 0; 70 -> the third block, slot 6).
+ * "vllm.models.flint.ops.decode_attention", flint_decode_attention
+ * parameters: seq_lens counts the KV positions including the current token, so
+ * with that convention the current token sits at seq_lens[b] - 1; for the MLA
+ * verify rows (decode_attention_fwd_verify parameters: a request's qlen verify
+ * tokens are its last qlen positions) row t of request b sits at
+ * seq_lens[b] - qlen + t.
+ *
+ * Readings: a request with no position to write (seq_lens <= 0, or a verify row
+ * before position 0) writes nothing; a position whose page entry is beyond the
+ * table or outside the cache writes nothing and is counted in *skipped.  An FP8
+ * cache stores e4m3(x / k_scale) with x / k_scale computed in fp32 (the
+ * precision the library computes it in) and rounded to the nearest e4m3 value,
+ * ties to even, saturating at +-448; -0 keeps its sign; NaN becomes 0x7F.
+ */
+
+/* float8 e4m3 "fn" encoding from the format's definition: normal values
+ * (1 + m/8) 2^(e-7) for e = 1..15 (e = 15, m = 7 is NaN, so the largest is
+ * 1.75 * 2^8 = 448), subnormals (m/8) 2^-6.  rint() rounds half to even in the
+ * default rounding mode; every product below is exact in double. */
+uint8_t pkv_oracle_f32_to_e4m3(float x) {
+    const double v = (double)x;
+    if (isnan(v)) return 0x7F;
+    const int s = signbit(v) ? 1 : 0;
+    const double a = fabs(v);
+    int code;
+    if (isinf(a)) {
+        code = 0x7E; /* saturates like any value beyond 448 */
+    } else if (a < ldexp(1.0, -6)) {
+        const double q = rint(a * 512.0); /* multiples of 2^-9: 0 .. 8 */
+        code = (q >= 8.0) ? (1 << 3) : (int)q;
+    } else {
+        int e;
+        const double f = frexp(a, &e); /* a = f 2^e, f in [0.5, 1) */
+        int E = e - 1;                 /* a = (2f) 2^E, 2f in [1, 2) */
+        double q = rint(16.0 * f);     /* 8 * (2f): 8 .. 16 */
+        if (q >= 16.0) {
+            q = 8.0;
+            E += 1;
+        }
+        if (E > 8 || (E == 8 && q > 14.0)) { /* beyond 448: saturate */
+            E = 8;
+            q = 14.0;
+        }
+        code = ((E + 7) << 3) | ((int)q - 8);
+    }
+    return (uint8_t)(code | (s << 7));
+}
+
+static int append_slot(const int32_t *bt, int64_t bt_sb, int64_t max_blocks, int64_t num_blocks,
+                       int64_t b, int64_t pos, int page_size, int64_t *blk, int64_t *slot) {
+    const int64_t pg = pos / page_size;
+    if (pg >= max_blocks) return 0;
+    const int64_t id = bt[b * bt_sb + pg];
+    if (id < 0 || id >= num_blocks) return 0;
+    *blk = id;
+    *slot = pos % page_size;
+    return 1;
+}
+
+/* k, v: [B, Hkv, D] bf16 (row strides src_sb, src_sh); kv: [num_blocks, Hkv,
+ * page, 2D] bf16 with K in [..., :D] and V in [..., D:]. */
+int pkv_oracle_gqa_kv_append(const uint16_t *k, const uint16_t *v, int64_t src_sb, int64_t src_sh,
+                             uint16_t *kv, int64_t kv_sblk, int64_t kv_sh, int64_t kv_stok,
+                             int64_t num_blocks, const int32_t *bt, int64_t bt_sb,
+                             int64_t max_blocks, const int32_t *seq_lens, int page_size,
+                             int64_t B, int64_t Hkv, int64_t D, int64_t *skipped) {
+    if (!k || !v || !kv || !bt || !seq_lens || page_size <= 0 || !skipped) return ORACLE_ERR_ARG;
+    *skipped = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        const int64_t L = seq_lens[b];
+        if (L <= 0) continue;
+        int64_t blk, slot;
+        if (!append_slot(bt, bt_sb, max_blocks, num_blocks, b, L - 1, page_size, &blk, &slot)) {
+            ++*skipped;
+            continue;
+        }
+        for (int64_t h = 0; h < Hkv; ++h) {
+            uint16_t *dst = kv + blk * kv_sblk + h * kv_sh + slot * kv_stok;
+            const uint16_t *ks = k + b * src_sb + h * src_sh;
+            const uint16_t *vs = v + b * src_sb + h * src_sh;
+            for (int64_t d = 0; d < D; ++d) {
+                dst[d] = ks[d];
+                dst[D + d] = vs[d];
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* latent: [B*qlen, Lk] bf16 (row stride lat_sr); cache: [num_pages, page, 1,
+ * Lk] bf16 (fp8 = 0) or e4m3 bytes (fp8 = 1); k_scale: the fp32 scale (FP8). */
+int pkv_oracle_mla_kv_append(const uint16_t *lat, int64_t lat_sr, void *cache, int fp8,
+                             int64_t c_spage, int64_t c_stok, int64_t num_pages, const int32_t *bt,
+                             int64_t bt_sb, int64_t max_blocks, const int32_t *seq_lens, int qlen,
+                             int page_size, float k_scale, int64_t B, int64_t Lk,
+                             int64_t *skipped) {
+    if (!lat || !cache || !bt || !seq_lens || page_size <= 0 || qlen < 1 || !skipped)
+        return ORACLE_ERR_ARG;
+    *skipped = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t t = 0; t < qlen; ++t) {
+            const int64_t pos = (int64_t)seq_lens[b] - qlen + t;
+            if (pos < 0) continue;
+            int64_t pg, slot;
+            if (!append_slot(bt, bt_sb, max_blocks, num_pages, b, pos, page_size, &pg, &slot)) {
+                ++*skipped;
+                continue;
+            }
+            const uint16_t *src = lat + (b * qlen + t) * lat_sr;
+            const int64_t at = pg * c_spage + slot * c_stok;
+            for (int64_t d = 0; d < Lk; ++d) {
+                if (fp8) {
+                    const float x = (float)pkv_oracle_bf16_to_f64(src[d]);
+                    ((uint8_t *)cache)[at + d] = pkv_oracle_f32_to_e4m3(x / k_scale);
+                } else {
+                    ((uint16_t *)cache)[at + d] = src[d];
+                }
+            }
+        }
+    }
+    return ORACLE_OK;
+}

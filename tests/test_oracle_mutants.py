@@ -129,3 +129,65 @@ def test_unmutated_oracle_passes_the_battery(monkeypatch):
             fn(oracle.load())
         else:
             fn(**kw)
+
+
+# ---- paged KV append and the e4m3 encoder --------------------------------
+import tests.test_oracle_append_pins as apins  # noqa: E402
+
+APPEND_MUTANTS = {
+    "append_position_is_seq_len": (
+        "if (!append_slot(bt, bt_sb, max_blocks, num_blocks, b, L - 1, page_size, &blk, &slot)) {",
+        "if (!append_slot(bt, bt_sb, max_blocks, num_blocks, b, L, page_size, &blk, &slot)) {"),
+    "append_slot_off_by_one": (
+        "    *slot = pos % page_size;",
+        "    *slot = (pos + 1) % page_size;"),
+    "mla_append_row_position": (
+        "const int64_t pos = (int64_t)seq_lens[b] - qlen + t;",
+        "const int64_t pos = (int64_t)seq_lens[b] - qlen + t + 1;"),
+    "append_writes_unassigned_pages": (
+        "    if (id < 0 || id >= num_blocks) return 0;",
+        "    if (id >= num_blocks) return 0;"),
+    "e4m3_encode_ties_away": (
+        "        double q = rint(16.0 * f);     /* 8 * (2f): 8 .. 16 */",
+        "        double q = round(16.0 * f);    /* 8 * (2f): 8 .. 16 */"),
+    "e4m3_encode_no_saturation": (
+        "        if (E > 8 || (E == 8 && q > 14.0)) { /* beyond 448: saturate */",
+        "        if (E > 9) { /* beyond 448: saturate */"),
+    "e4m3_encode_subnormal_step": (
+        "        const double q = rint(a * 512.0); /* multiples of 2^-9: 0 .. 8 */",
+        "        const double q = rint(a * 256.0); /* multiples of 2^-9: 0 .. 8 */"),
+    "fp8_append_multiplies_by_k_scale": (
+        "pkv_oracle_f32_to_e4m3(x / k_scale);",
+        "pkv_oracle_f32_to_e4m3(x * k_scale);"),
+}
+
+APPEND_BATTERY = [
+    (apins.test_gqa_append_worked_example, {}),
+    (apins.test_mla_append_worked_example, dict(qlen=1)),
+    (apins.test_mla_append_worked_example, dict(qlen=2)),
+    (apins.test_append_skips_rows_without_a_position_or_page, {}),
+    (apins.test_e4m3_encode_round_trips_every_code, {}),
+    (apins.test_e4m3_encode_ties_to_even_and_saturates, {}),
+    (apins.test_e4m3_encode_matches_torch_in_range, {}),
+    (apins.test_mla_fp8_append_stores_e4m3_of_x_over_k_scale, {}),
+]
+
+
+@pytest.mark.parametrize("name", sorted(APPEND_MUTANTS))
+def test_append_mutant_is_caught(name, monkeypatch):
+    old, new = APPEND_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutant {name}: pattern must occur exactly once"
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, f"{name}.c")
+        with open(path, "w") as f:
+            f.write(src.replace(old, new))
+        lib = oracle.load(oracle.compile_oracle(path, os.path.join(tmp, f"lib{name}.so")))
+        monkeypatch.setattr(apins, "LIB", lib)
+        caught = []
+        for fn, kw in APPEND_BATTERY:
+            try:
+                fn(**kw)
+            except (AssertionError, oracle.OracleError):
+                caught.append(fn.__name__)
+        assert caught, f"no pin catches mutant {name}"
