@@ -259,8 +259,9 @@ def _tiny(dev, flush, steps, tiny, gqa_entry):
 def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
     """Every other workload of the pages' problem, timed the same way (inputs
     resident, L2 flushed between calls, CUDA events): the tiny decode batch,
-    the 131072-token long context at B=1 and B=8 across split caps, and the
-    two MLA verify workloads (bf16 and FP8 latent caches)."""
+    the 131072-token long context at B=1 and B=8 across split caps, the two
+    MLA verify workloads (bf16 and FP8 latent caches) and the paged KV append
+    that precedes a decode or verify call."""
     import torch
     import paged_kv_cache_30_gb300 as pkv
     from paged_kv_cache_30_gb300 import workloads as W
@@ -317,6 +318,29 @@ def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
                      "GBps": nbytes / (med * 1e-3) / 1e9, "flops": fl, "kv_bytes": nbytes,
                      "cap": prob.num_kv_splits}
         del tq, tc
+    if want("append"):
+        # the cache write before each call: the Flint batch's current tokens
+        # (64 x 8 kv heads x 512 B) and the MLA verify rows (32 x 4 x 1152 B)
+        prob = W.flint_gqa(0, 0)
+        B, Hq = prob.q.shape[:2]
+        k = W.normal((B, Hq // 8, 128), 91).to(dev)
+        v = W.normal((B, Hq // 8, 128), 92).to(dev)
+        kv, bt, sl = prob.kv_cache.to(dev), prob.block_table.to(dev), prob.seq_lens.to(dev)
+        fn = lambda: pkv.gqa_kv_append(k, v, kv, bt, sl, prob.page_size)
+        med, _ = time_events(fn, flush, steps)
+        nbytes = 2 * int((prob.seq_lens > 0).sum()) * (Hq // 8) * 512  # read + written
+        res["kv_append_flint_b64"] = {"us": 1e3 * med, "GBps": nbytes / (med * 1e-3) / 1e9,
+                                      "rows": int((prob.seq_lens > 0).sum()) * (Hq // 8)}
+        del kv
+        mp = W.mla_verify(0)
+        lat = W.normal((mp.q.shape[0], 576), 93).to(dev)
+        cache, mbt, msl = mp.latent_cache.to(dev), mp.block_table.to(dev), mp.seq_lens.to(dev)
+        fn = lambda: pkv.mla_kv_append(lat, cache, mbt, msl, mp.qlen, mp.page_size)
+        med, _ = time_events(fn, flush, steps)
+        nbytes = 2 * mp.q.shape[0] * 1152
+        res["kv_append_mla_b32_q4"] = {"us": 1e3 * med, "GBps": nbytes / (med * 1e-3) / 1e9,
+                                       "rows": int(mp.q.shape[0])}
+        del cache
     assert pkv.check_errors(dev.index or 0) == 0
     return res
 
@@ -564,7 +588,7 @@ def main():
                     help="skip the other workloads (tiny, long context, MLA)")
     ap.add_argument("--extra-steps", type=int, default=30)
     ap.add_argument("--only", default="",
-                    help="comma list of tiny,long1,long8,mla,mla_fp8: time only these (no headline)")
+                    help="comma list of tiny,long1,long8,mla,mla_fp8,append: time only these (no headline)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -1,7 +1,8 @@
 /*
  * pkv.h -- C ABI of libpkv: split-KV paged decode attention on GB300 (sm_103a).
  *
- * Two operations, each one kernel launch on the caller's stream:
+ * Two attention operations and the cache write that precedes them, each one
+ * kernel launch on the caller's stream:
  *
  *  - pkv_paged_decode_attn: GQA decode.  Every request has one query token per
  *    query head; it attends to the keys of its KV cache, gathered page by page
@@ -19,7 +20,12 @@
  *    "vllm.v1.attention.ops.triton_decode_attention"
  *    (decode_attention_fwd_verify: parameters).
  *
- * Both compute the fp32 online softmax of the pages (exp2 with the softmax
+ *  - pkv_gqa_kv_append / pkv_mla_kv_append: the step before either call,
+ *    writing the current token (or the verify tokens' latent rows) into the
+ *    paged cache in place through the same block table (transformers page,
+ *    decode path).
+ *
+ * Both attention calls compute the fp32 online softmax of the pages (exp2 with the softmax
  * scale folded into log2(e), P rounded to bf16 for P.V, fp32 accumulation),
  * split each request's keys over several CTAs, and merge the fp32
  * (unnormalised O, running max m, sum l) partials of the splits into a bf16
@@ -227,6 +233,66 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
 PKV_API int pkv_num_kv_splits(int max_seq_len, int batch, int qlen, int num_heads, int sm_count,
                               int block_h, double occupancy, int min_work_per_split,
                               int max_splits);
+
+/*
+ * pkv_gqa_kv_append -- write each request's current token into the paged GQA
+ * cache, in place, before the decode call reads it.
+ * Source: "Atencion paginada" (transformers), decode path, "Comportamiento de
+ * la cache" and "Ejemplo" (the cache is updated in place through block_table:
+ * a sequence with n cached tokens puts its new token at logical position n);
+ * position convention of "vllm.models.flint.ops.decode_attention",
+ * flint_decode_attention parameters (seq_lens counts the current token).
+ *
+ *   k, v          bf16 [B, Hkv, 128], last dim contiguous, 16-byte aligned rows
+ *                 (strides % 8 == 0): the current token's key and value.
+ *   kv_cache      bf16 [num_blocks, Hkv, P, 256] as for pkv_paged_decode_attn;
+ *                 K goes to [..., :128], V to [..., 128:].  Written in place.
+ *   block_table   int32 [B, max_blocks].
+ *   seq_lens      int32 [B], lengths including the current token: the token is
+ *                 written at position seq_lens[b] - 1, i.e. page
+ *                 block_table[b][pos / P], slot pos % P.  seq_lens[b] <= 0
+ *                 writes nothing.
+ *   page_size     P (16 or 32).
+ *   stream        cudaStream_t.
+ * A position whose page entry lies beyond max_blocks or outside
+ * [0, num_blocks) is not written; it raises bit 2 or bit 1 of the device error
+ * word (pkv_check_errors).  Nothing else of the cache changes.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_ALIGNMENT, PKV_ERR_UNSUPPORTED (shapes,
+ * strides, dtypes, page size) before any CUDA call; PKV_ERR_CUDA on a failed
+ * launch.  B == 0 is a no-op.  Only the device error word of the workspace
+ * is used (the workspace is allocated on first use, as for the attention
+ * calls).
+ */
+PKV_API int pkv_gqa_kv_append(const pkv_tensor* k, const pkv_tensor* v, const pkv_tensor* kv_cache,
+                              const pkv_tensor* block_table, const pkv_tensor* seq_lens,
+                              int page_size, void* stream);
+
+/*
+ * pkv_mla_kv_append -- write the latent rows of each request's verify tokens
+ * into the paged latent cache, in place.
+ * Source: as pkv_gqa_kv_append, with the verify layout of
+ * "vllm.v1.attention.ops.triton_decode_attention", decode_attention_fwd_verify
+ * (parameters): a request's qlen verify tokens are its last qlen positions.
+ *
+ *   latent        bf16 [B*qlen, 576] (row r = b*qlen + t), last dim contiguous,
+ *                 16-byte aligned rows.
+ *   latent_cache  bf16 or FP8 e4m3 [num_pages, P, 1, 576] (or
+ *                 [num_pages*P, 1, 576]), as for pkv_mla_verify_attn.
+ *   block_table   int32 [B, max_pages].
+ *   seq_lens      int32 [B]: row t of request b goes to position
+ *                 seq_lens[b] - qlen + t (nothing when negative).
+ *   qlen          verify tokens per request (>= 1).
+ *   page_size     P (16 or 32).
+ *   k_scale       fp32 device scalar, or NULL (= 1).  An e4m3 cache stores
+ *                 e4m3(x / k_scale): the quotient in fp32 (IEEE division),
+ *                 then the nearest e4m3 value, ties to even, saturating at
+ *                 +-448.  Ignored for a bf16 cache (rows are copied).
+ *   stream        cudaStream_t.
+ * Bad table entries and error codes as for pkv_gqa_kv_append.
+ */
+PKV_API int pkv_mla_kv_append(const pkv_tensor* latent, const pkv_tensor* latent_cache,
+                              const pkv_tensor* block_table, const pkv_tensor* seq_lens, int qlen,
+                              int page_size, const pkv_tensor* k_scale, void* stream);
 
 /*
  * pkv_check_errors -- read and clear the device error word of `device`

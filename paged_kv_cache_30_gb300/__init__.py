@@ -14,6 +14,9 @@ Names follow the C ABI without its ``pkv_`` prefix:
     mla_verify_attn(q, latent_cache, block_table, seq_lens, real_seq_lens, qlen,
                     scale, page_size, k_scale, out, lse, num_kv_splits=0,
                     stream=None)
+    gqa_kv_append(k, v, kv_cache, block_table, seq_lens, page_size, stream=None)
+    mla_kv_append(latent, latent_cache, block_table, seq_lens, qlen, page_size,
+                  k_scale=None, stream=None)
     num_kv_splits(max_seq_len, batch, qlen, num_heads, sm_count, ...)
     init(device, workspace_bytes=0), check_errors(device),
     check_counters(device), shutdown(), version()
@@ -28,7 +31,7 @@ import threading
 __all__ = [
     "PkvError", "load_library", "library_path", "init", "paged_decode_attn",
     "paged_decode_attn_noalloc",
-    "mla_verify_attn", "num_kv_splits", "check_errors", "check_counters", "shutdown",
+    "mla_verify_attn", "gqa_kv_append", "mla_kv_append", "num_kv_splits", "check_errors", "check_counters", "shutdown",
     "version", "last_error",
 ]
 
@@ -84,12 +87,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.pkv_paged_decode_attn.argtypes = [T, T, T, T, T, i32, f32, i32, i32, T, T, vp]
         lib.pkv_paged_decode_attn_noalloc.argtypes = [T, T, T, T, T, i32, f32, i32, i32, T, T, vp]
         lib.pkv_mla_verify_attn.argtypes = [T, T, T, T, T, i32, f32, i32, T, T, T, i32, vp]
+        lib.pkv_gqa_kv_append.argtypes = [T, T, T, T, T, i32, vp]
+        lib.pkv_mla_kv_append.argtypes = [T, T, T, T, i32, i32, T, vp]
         lib.pkv_num_kv_splits.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_double, i32, i32]
         lib.pkv_check_errors.argtypes = [i32, ctypes.POINTER(ctypes.c_int32)]
         lib.pkv_check_counters.argtypes = [i32, ctypes.POINTER(ctypes.c_int64)]
         lib.pkv_last_error.restype = ctypes.c_char_p
         for name in ("pkv_init", "pkv_paged_decode_attn", "pkv_paged_decode_attn_noalloc",
-                     "pkv_mla_verify_attn",
+                     "pkv_mla_verify_attn", "pkv_gqa_kv_append", "pkv_mla_kv_append",
                      "pkv_num_kv_splits", "pkv_check_errors", "pkv_check_counters",
                      "pkv_shutdown", "pkv_version"):
             getattr(lib, name).restype = i32
@@ -191,6 +196,27 @@ def mla_verify_attn(q, latent_cache, block_table, seq_lens, real_seq_lens, qlen,
         _desc(real_seq_lens), int(qlen), float(scale), int(page_size), _desc(k_scale),
         _desc(out), _desc(lse), int(num_kv_splits), _stream(stream, q)))
     return out
+
+
+def gqa_kv_append(k, v, kv_cache, block_table, seq_lens, page_size, stream=None):
+    """Write each request's current token (position seq_lens[b] - 1) into the
+    paged GQA cache in place (C: pkv_gqa_kv_append).  Returns ``kv_cache``."""
+    lib = load_library()
+    _check(lib.pkv_gqa_kv_append(_desc(k), _desc(v), _desc(kv_cache), _desc(block_table),
+                                 _desc(seq_lens), int(page_size), _stream(stream, k)))
+    return kv_cache
+
+
+def mla_kv_append(latent, latent_cache, block_table, seq_lens, qlen, page_size, k_scale=None,
+                  stream=None):
+    """Write verify row t of request b (position seq_lens[b] - qlen + t) into
+    the paged latent cache in place; an e4m3 cache stores e4m3(x / k_scale)
+    (C: pkv_mla_kv_append).  Returns ``latent_cache``."""
+    lib = load_library()
+    _check(lib.pkv_mla_kv_append(_desc(latent), _desc(latent_cache), _desc(block_table),
+                                 _desc(seq_lens), int(qlen), int(page_size), _desc(k_scale),
+                                 _stream(stream, latent)))
+    return latent_cache
 
 
 def num_kv_splits(max_seq_len, batch, qlen, num_heads, sm_count, block_h=64, occupancy=1.0,

@@ -631,6 +631,165 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
   return PKV_OK;
 }
 
+PKV_API int pkv_gqa_kv_append(const pkv_tensor* k, const pkv_tensor* v, const pkv_tensor* kv_cache,
+                              const pkv_tensor* block_table, const pkv_tensor* seq_lens,
+                              int page_size, void* stream_ptr) {
+  int rc;
+  if ((rc = check_tensor(k, "k", PKV_DTYPE_BF16, 3))) return rc;
+  if ((rc = check_tensor(v, "v", PKV_DTYPE_BF16, 3))) return rc;
+  if ((rc = check_tensor(kv_cache, "kv_cache", PKV_DTYPE_BF16, 4))) return rc;
+  if ((rc = check_tensor(block_table, "block_table", PKV_DTYPE_I32, 2))) return rc;
+  if ((rc = check_tensor(seq_lens, "seq_lens", PKV_DTYPE_I32, 1))) return rc;
+  const int64_t B = k->shape[0], Hkv = k->shape[1], D = k->shape[2];
+  const int64_t nb = kv_cache->shape[0];
+  if (D != pkv::kGqaHeadDim)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %lld (only 128 is built)", (long long)D);
+  if (v->shape[0] != B || v->shape[1] != Hkv || v->shape[2] != D)
+    return fail(PKV_ERR_INVALID_ARG, "v must have the shape of k");
+  if (kv_cache->shape[1] != Hkv || kv_cache->shape[3] != 2 * D)
+    return fail(PKV_ERR_INVALID_ARG, "kv_cache must be [num_blocks, Hkv, P, 256]");
+  if (page_size != 16 && page_size != 32)
+    return fail(PKV_ERR_UNSUPPORTED, "page_size %d (16 and 32 are built)", page_size);
+  if (kv_cache->shape[2] != page_size)
+    return fail(PKV_ERR_INVALID_ARG, "kv_cache.shape[2] %lld != page_size %d",
+                (long long)kv_cache->shape[2], page_size);
+  if (nb < 1 || nb >= (int64_t(1) << 31))
+    return fail(PKV_ERR_INVALID_ARG, "num_blocks %lld", (long long)nb);
+  if (block_table->shape[0] != B || seq_lens->shape[0] != B)
+    return fail(PKV_ERR_INVALID_ARG, "block_table / seq_lens batch mismatch");
+  if (block_table->shape[1] < 1 || block_table->shape[1] > (int64_t(1) << 30) ||
+      (block_table->stride[1] != 1 && block_table->shape[1] > 1))
+    return fail(PKV_ERR_INVALID_ARG, "block_table rows must be non-empty and contiguous");
+  if (seq_lens->stride[0] != 1 && B > 1)
+    return fail(PKV_ERR_INVALID_ARG, "seq_lens must be contiguous");
+  if (k->stride[2] != 1 || v->stride[2] != 1 || kv_cache->stride[3] != 1)
+    return fail(PKV_ERR_INVALID_ARG, "k/v last dim and kv_cache rows must be contiguous");
+  if (k->stride[0] != v->stride[0] || k->stride[1] != v->stride[1])
+    return fail(PKV_ERR_INVALID_ARG, "k and v must share strides");
+  if (k->stride[0] % 8 || k->stride[1] % 8 || kv_cache->stride[0] % 8 ||
+      kv_cache->stride[1] % 8 || kv_cache->stride[2] % 8)
+    return fail(PKV_ERR_ALIGNMENT, "strides of k, v and kv_cache must be multiples of 8");
+  if (!aligned16(k->data) || !aligned16(v->data) || !aligned16(kv_cache->data))
+    return fail(PKV_ERR_ALIGNMENT, "k, v and kv_cache must be 16-byte aligned");
+  if (B == 0) return PKV_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int dev = 0;
+  DeviceState* st = nullptr;
+  bool capturing = false;
+  if ((rc = workspace_for(stream, &dev, &st, &capturing))) return rc;
+  pkv::AppendParams p;
+  std::memset(&p, 0, sizeof p);
+  p.k = static_cast<const uint16_t*>(k->data);
+  p.v = static_cast<const uint16_t*>(v->data);
+  p.s_sb = k->stride[0];
+  p.s_sh = k->stride[1];
+  p.cache = static_cast<uint8_t*>(kv_cache->data);
+  p.c_sblk = kv_cache->stride[0] * 2;
+  p.c_sh = kv_cache->stride[1] * 2;
+  p.c_stok = kv_cache->stride[2] * 2;
+  p.num_blocks = int(nb);
+  p.bt = static_cast<const int32_t*>(block_table->data);
+  p.bt_sb = block_table->stride[0];
+  p.max_blocks = int(block_table->shape[1]);
+  p.seq_lens = static_cast<const int32_t*>(seq_lens->data);
+  p.B = int(B);
+  p.Hkv = int(Hkv);
+  p.qlen = 1;
+  p.page_size = page_size;
+  p.err = st->ws.err;
+  if (B * Hkv >= (int64_t(1) << 31)) return fail(PKV_ERR_UNSUPPORTED, "B x Hkv too large");
+  const cudaError_t e = pkv::launch_gqa_kv_append(p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gqa kv append launch");
+  return PKV_OK;
+}
+
+PKV_API int pkv_mla_kv_append(const pkv_tensor* latent, const pkv_tensor* latent_cache,
+                              const pkv_tensor* block_table, const pkv_tensor* seq_lens, int qlen,
+                              int page_size, const pkv_tensor* k_scale, void* stream_ptr) {
+  int rc;
+  if ((rc = check_tensor(latent, "latent", PKV_DTYPE_BF16, 2))) return rc;
+  if (!latent_cache) return fail(PKV_ERR_INVALID_ARG, "latent_cache is NULL");
+  const bool fp8 = latent_cache->dtype == PKV_DTYPE_FP8_E4M3;
+  if ((rc = check_tensor(latent_cache, "latent_cache", fp8 ? PKV_DTYPE_FP8_E4M3 : PKV_DTYPE_BF16,
+                         latent_cache->ndim == 4 ? 4 : 3)))
+    return rc;
+  if ((rc = check_tensor(block_table, "block_table", PKV_DTYPE_I32, 2))) return rc;
+  if ((rc = check_tensor(seq_lens, "seq_lens", PKV_DTYPE_I32, 1))) return rc;
+  if (k_scale) {
+    if ((rc = check_tensor(k_scale, "k_scale", PKV_DTYPE_F32, k_scale->ndim))) return rc;
+    if (!(k_scale->ndim == 0 || (k_scale->ndim == 1 && k_scale->shape[0] == 1)))
+      return fail(PKV_ERR_INVALID_ARG, "k_scale must be an fp32 scalar on the device");
+  }
+  if (qlen < 1) return fail(PKV_ERR_INVALID_ARG, "qlen %d < 1", qlen);
+  const int64_t R = latent->shape[0], Lk = latent->shape[1];
+  if (Lk != pkv::kMlaLk) return fail(PKV_ERR_UNSUPPORTED, "Lk %lld (576 is built)", (long long)Lk);
+  if (R % qlen) return fail(PKV_ERR_INVALID_ARG, "latent rows %lld not a multiple of qlen %d",
+                            (long long)R, qlen);
+  const int64_t B = R / qlen;
+  if (page_size != 16 && page_size != 32)
+    return fail(PKV_ERR_UNSUPPORTED, "page_size %d (16 and 32 are built)", page_size);
+  int64_t num_pages, s_page, s_tok;
+  if (latent_cache->ndim == 4) {
+    if (latent_cache->shape[1] != page_size || latent_cache->shape[2] != 1 ||
+        latent_cache->shape[3] != Lk || latent_cache->stride[3] != 1)
+      return fail(PKV_ERR_INVALID_ARG, "latent_cache must be [num_pages, %d, 1, 576], rows contiguous",
+                  page_size);
+    num_pages = latent_cache->shape[0];
+    s_page = latent_cache->stride[0];
+    s_tok = latent_cache->stride[1];
+  } else {
+    if (latent_cache->shape[1] != 1 || latent_cache->shape[2] != Lk ||
+        latent_cache->shape[0] % page_size || latent_cache->stride[2] != 1)
+      return fail(PKV_ERR_INVALID_ARG, "latent_cache must be [num_pages * P, 1, 576], rows contiguous");
+    num_pages = latent_cache->shape[0] / page_size;
+    s_tok = latent_cache->stride[0];
+    s_page = s_tok * page_size;
+  }
+  const int esz = fp8 ? 1 : 2;
+  if (num_pages < 1 || num_pages >= (int64_t(1) << 31))
+    return fail(PKV_ERR_INVALID_ARG, "num_pages %lld", (long long)num_pages);
+  if ((s_tok * esz) % 16 || (s_page * esz) % 16 || !aligned16(latent_cache->data))
+    return fail(PKV_ERR_ALIGNMENT, "latent cache rows and pages must be 16-byte aligned");
+  if (latent->stride[1] != 1 || latent->stride[0] % 8 || !aligned16(latent->data))
+    return fail(PKV_ERR_ALIGNMENT, "latent rows must be contiguous and 16-byte aligned");
+  if (block_table->shape[0] != B || seq_lens->shape[0] != B)
+    return fail(PKV_ERR_INVALID_ARG, "block_table / seq_lens batch mismatch");
+  if (block_table->shape[1] < 1 || block_table->shape[1] > (int64_t(1) << 30) ||
+      (block_table->stride[1] != 1 && block_table->shape[1] > 1))
+    return fail(PKV_ERR_INVALID_ARG, "block_table rows must be non-empty and contiguous");
+  if (seq_lens->stride[0] != 1 && B > 1)
+    return fail(PKV_ERR_INVALID_ARG, "seq_lens must be contiguous");
+  if (R >= (int64_t(1) << 31)) return fail(PKV_ERR_UNSUPPORTED, "too many latent rows");
+  if (B == 0) return PKV_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int dev = 0;
+  DeviceState* st = nullptr;
+  bool capturing = false;
+  if ((rc = workspace_for(stream, &dev, &st, &capturing))) return rc;
+  pkv::AppendParams p;
+  std::memset(&p, 0, sizeof p);
+  p.k = static_cast<const uint16_t*>(latent->data);
+  p.s_sb = latent->stride[0];
+  p.cache = static_cast<uint8_t*>(latent_cache->data);
+  p.c_sblk = s_page * esz;
+  p.c_stok = s_tok * esz;
+  p.num_blocks = int(num_pages);
+  p.bt = static_cast<const int32_t*>(block_table->data);
+  p.bt_sb = block_table->stride[0];
+  p.max_blocks = int(block_table->shape[1]);
+  p.seq_lens = static_cast<const int32_t*>(seq_lens->data);
+  p.B = int(B);
+  p.Hkv = 1;
+  p.qlen = qlen;
+  p.page_size = page_size;
+  p.fp8 = fp8 ? 1 : 0;
+  p.k_scale = (fp8 && k_scale) ? static_cast<const float*>(k_scale->data) : nullptr;
+  p.err = st->ws.err;
+  const cudaError_t e = pkv::launch_mla_kv_append(p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "mla kv append launch");
+  return PKV_OK;
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------------------------

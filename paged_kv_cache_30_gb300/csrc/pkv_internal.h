@@ -127,6 +127,26 @@ struct MlaParams {
 cudaError_t launch_mla_verify(const MlaParams& p, const CUtensorMap& q_map,
                               const CUtensorMap& kv_map, bool fp8, int grid, cudaStream_t stream);
 
+// ---------------------------------------------------------- KV append --
+struct AppendParams {
+  const uint16_t* k;     // GQA: k [B, Hkv, 128]; MLA: latent [B*qlen, 576]
+  const uint16_t* v;     // GQA: v [B, Hkv, 128]; MLA: unused
+  int64_t s_sb, s_sh;    // source strides (elements): GQA [b, h]; MLA [row, -]
+  uint8_t* cache;        // cache base
+  int64_t c_sblk, c_sh, c_stok;  // bytes: block/page, kv head (GQA), token
+  int num_blocks;
+  const int32_t* bt;
+  int64_t bt_sb;
+  int max_blocks;
+  const int32_t* seq_lens;
+  int B, Hkv, qlen, page_size;
+  int fp8;               // MLA: e4m3 cache
+  const float* k_scale;  // MLA FP8: device scalar or null
+  int* err;
+};
+cudaError_t launch_gqa_kv_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_mla_kv_append(const AppendParams& p, cudaStream_t stream);
+
 // The counter region of the workspace holds 2^20 ints: the first half for
 // (request, kv head) counters, the second half for split-group counters.
 constexpr int64_t kTopCounters = int64_t(1) << 19;

@@ -144,3 +144,53 @@ def test_num_kv_splits_clamps():
 
 def test_mla_entry_point_is_exported(lib):
     assert hasattr(lib, "pkv_mla_verify_attn")
+
+
+# ------------------------------------------------------------- KV append --
+def _append_args(B=2, Hkv=2, P=16, nb=64, maxb=8):
+    return dict(k=_t([B, Hkv, 128], pkv.DTYPE_BF16), v=_t([B, Hkv, 128], pkv.DTYPE_BF16, ptr=0x20000),
+                kv=_t([nb, Hkv, P, 256], pkv.DTYPE_BF16, ptr=0x30000),
+                bt=_t([B, maxb], pkv.DTYPE_I32), sl=_t([B], pkv.DTYPE_I32))
+
+
+def _append(lib, a, P=16):
+    r = ctypes.byref
+    return lib.pkv_gqa_kv_append(r(a["k"]), r(a["v"]), r(a["kv"]), r(a["bt"]), r(a["sl"]), P, None)
+
+
+@pytest.mark.parametrize("mutate,P,code", [
+    (lambda a: a.update(k=_t([2, 2, 64], pkv.DTYPE_BF16)), 16, -2),               # head dim
+    (lambda a: a.update(v=_t([2, 3, 128], pkv.DTYPE_BF16)), 16, -1),              # v shape
+    (lambda a: a.update(kv=_t([64, 4, 16, 256], pkv.DTYPE_BF16)), 16, -1),        # Hkv
+    (lambda a: None, 8, -2),                                                       # page size
+    (lambda a: None, 32, -1),                                                      # P != shape[2]
+    (lambda a: a.update(k=_t([2, 2, 128], pkv.DTYPE_BF16, ptr=0x10004)), 16, -3),  # alignment
+    (lambda a: a.update(sl=_t([3], pkv.DTYPE_I32)), 16, -1),                      # batch
+    (lambda a: a.update(k=_t([2, 2, 128], pkv.DTYPE_F32)), 16, -1),               # dtype
+])
+def test_gqa_append_validation_rejects_before_any_cuda_call(lib, mutate, P, code):
+    a = _append_args()
+    mutate(a)
+    assert _append(lib, a, P) == code
+    assert pkv.last_error()
+
+
+def test_gqa_append_empty_batch_is_a_no_op(lib):
+    assert _append(lib, _append_args(B=0)) == 0
+
+
+def test_mla_append_validation(lib):
+    r = ctypes.byref
+    lat = _t([8, 576], pkv.DTYPE_BF16)
+    cache = _t([32, 16, 1, 576], pkv.DTYPE_FP8, ptr=0x40000)
+    bt, sl = _t([4, 8], pkv.DTYPE_I32), _t([4], pkv.DTYPE_I32)
+    ks = _t([], pkv.DTYPE_F32, ptr=0x50000)
+    assert lib.pkv_mla_kv_append(r(lat), r(cache), r(bt), r(sl), 3, 16, r(ks), None) == -1  # 8 % 3
+    assert lib.pkv_mla_kv_append(r(lat), r(cache), r(bt), r(sl), 2, 64, r(ks), None) == -2  # page
+    bad = _t([8, 512], pkv.DTYPE_BF16)
+    assert lib.pkv_mla_kv_append(r(bad), r(cache), r(bt), r(sl), 2, 16, r(ks), None) == -2  # Lk
+    ks2 = _t([2], pkv.DTYPE_F32, ptr=0x50000)
+    assert lib.pkv_mla_kv_append(r(lat), r(cache), r(bt), r(sl), 2, 16, r(ks2), None) == -1
+    empty = _t([0, 576], pkv.DTYPE_BF16)
+    bt0, sl0 = _t([0, 8], pkv.DTYPE_I32), _t([0], pkv.DTYPE_I32)
+    assert lib.pkv_mla_kv_append(r(empty), r(cache), r(bt0), r(sl0), 2, 16, None, None) == 0
