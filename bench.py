@@ -401,6 +401,27 @@ def run_reference(args, rank, world):
 
 
 # --------------------------------------------------------------- main arm --
+# ------------------------------------------------- ranks (weak scaling) ---
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank runs its own batch: same shapes and length law, its own draw."""
+    return seed + 7919 * rank
+
+
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The slowest rank's value (all ranks receive it); x itself on one rank."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, step_bytes: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's step time."""
+    return world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import paged_kv_cache_30_gb300 as pkv
@@ -429,7 +450,7 @@ def run_gpu(args, rank, world, local_rank):
         return
 
     # weak scaling: every rank runs its own batch of 64 requests
-    layers = make_layers(args.seed + 7919 * rank)
+    layers = make_layers(rank_seed(args.seed, rank))
     kv_bytes = [p.kv_bytes() for p in layers]
     step_bytes = sum(kv_bytes)
     stream = torch.cuda.current_stream(dev)
@@ -478,13 +499,9 @@ def run_gpu(args, rank, world, local_rank):
     sampler.stop()
     full_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
     step_ms = [ev[s][0].elapsed_time(ev[s][2]) for s in range(args.steps)]
-    total_ms = sum(step_ms)
-    if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     ms_per_step = total_ms / args.steps
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = job_value(world, step_bytes, ms_per_step)
     calls_per_s = world * 2 / (ms_per_step * 1e-3)
     full_mean = statistics.mean(full_ms)
     achieved = kv_bytes[0] / (full_mean * 1e-3) / 1e9
@@ -515,12 +532,8 @@ def run_gpu(args, rank, world, local_rank):
         e2e_ev[s][1].record(stream)
         flush.fill_(float(s & 7))
     barrier()
-    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in e2e_ev)
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = world * step_bytes / (e2e_ms / args.steps * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in e2e_ev), dist, dev)
+    e2e_value = job_value(world, step_bytes, e2e_ms / args.steps)
     assert pkv.check_errors(local_rank) == 0
 
     if dist:
