@@ -423,6 +423,7 @@ def job_value(world: int, step_bytes: int, ms_per_step: float) -> float:
 
 
 def run_gpu(args, rank, world, local_rank):
+    import numpy as np
     import torch
     import paged_kv_cache_30_gb300 as pkv
     from paged_kv_cache_30_gb300 import build as pkv_build
@@ -509,31 +510,86 @@ def run_gpu(args, rank, world, local_rank):
     assert pkv.check_errors(local_rank) == 0
 
     # ---------------- end to end through the same call, host buffers ----------------
-    hq = [p.q.pin_memory() for p in layers]
-    hbt = layers[0].block_table.pin_memory()
-    hsl = layers[0].seq_lens.pin_memory()
-    hout = [torch.empty(p.q.shape, dtype=torch.bfloat16).pin_memory() for p in layers]
-    hlse = [torch.empty(p.q.shape[:2], dtype=torch.float32).pin_memory() for p in layers]
-    h2d = sum(x.numel() * x.element_size() for x in hq) + hbt.numel() * 4 + hsl.numel() * 4
-    d2h = sum(x.numel() * x.element_size() for x in hout) + sum(x.numel() * 4 for x in hlse)
-    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    # Every step copies its inputs (q of both layers, block table, seq_lens)
+    # from pinned host memory and reads its results (out, lse of both layers)
+    # back; the copies run on a second stream, double-buffered, so step s+1's
+    # upload and step s's download overlap step s's kernels.  No flush inside
+    # this loop: each step streams 777 MB of KV, more than the 129 MB L2.
+    # one pinned upload buffer per step: [q of layer 0 | q of layer 1 | block table |
+    # seq_lens]; one download buffer: [out 0 | out 1 | lse 0 | lse 1]
+    def carve(buf, specs):
+        views, off = [], 0
+        for shape, dtype in specs:
+            nbytes = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+            views.append(buf[off:off + nbytes].view(dtype).view(shape))
+            off += (nbytes + 255) // 256 * 256
+        return views
+    in_specs = [(tuple(p.q.shape), torch.bfloat16) for p in layers] + [
+        (tuple(layers[0].block_table.shape), torch.int32), (tuple(layers[0].seq_lens.shape), torch.int32)]
+    out_specs = [(tuple(p.q.shape), torch.bfloat16) for p in layers] + [
+        (tuple(p.q.shape[:2]), torch.float32) for p in layers]
+    def size_of(specs):
+        return sum((int(np.prod(sh)) * torch.tensor([], dtype=dt).element_size() + 255) // 256 * 256
+                   for sh, dt in specs)
+    h_in = torch.empty(size_of(in_specs), dtype=torch.uint8).pin_memory()
+    hv = carve(h_in, in_specs)
+    for i in range(2):
+        hv[i].copy_(layers[i].q)
+    hv[2].copy_(layers[0].block_table)
+    hv[3].copy_(layers[0].seq_lens)
+    d_in = [torch.empty_like(h_in, device=dev) for _ in range(2)]
+    dv = [carve(x, in_specs) for x in d_in]
+    h_out = [torch.empty(size_of(out_specs), dtype=torch.uint8).pin_memory() for _ in range(2)]
+    hov = [carve(x, out_specs) for x in h_out]
+    d_out = [torch.empty_like(h_out[0], device=dev) for _ in range(2)]
+    dov = [carve(x, out_specs) for x in d_out]
+    h2d = sum(int(np.prod(sh)) * torch.tensor([], dtype=dt).element_size() for sh, dt in in_specs)
+    d2h = sum(int(np.prod(sh)) * torch.tensor([], dtype=dt).element_size() for sh, dt in out_specs)
+    copy = torch.cuda.Stream(dev)
+    up = [torch.cuda.Event() for _ in range(2)]      # inputs of buffer b uploaded
+    done = [torch.cuda.Event() for _ in range(2)]    # kernels of buffer b finished
+    down = [torch.cuda.Event() for _ in range(2)]    # outputs of buffer b read back
+
+    def e2e_step(s):
+        b = s & 1
+        with torch.cuda.stream(copy):
+            if s >= 2:
+                copy.wait_event(done[b])             # step s-2 no longer reads buffer b
+            d_in[b].copy_(h_in, non_blocking=True)
+            up[b].record(copy)
+        stream.wait_event(up[b])
+        if s >= 2:
+            stream.wait_event(down[b])               # step s-2's results are read back
+        for i in range(2):
+            p = layers[i]
+            pkv.paged_decode_attn(dv[b][i], d[i]["kv"], dv[b][2], dv[b][3], d[i]["sinks"],
+                                  p.window, p.scale, 16, 0, dov[b][i], dov[b][2 + i],
+                                  stream=stream)
+        done[b].record(stream)
+        with torch.cuda.stream(copy):
+            copy.wait_event(done[b])
+            h_out[b].copy_(d_out[b], non_blocking=True)
+            down[b].record(copy)
+
+    for s in range(3):  # warm the copy path
+        e2e_step(s)
+    torch.cuda.synchronize()
     barrier()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
     for s in range(args.steps):
-        e2e_ev[s][0].record(stream)
-        for i in range(2):
-            d[i]["q"].copy_(hq[i], non_blocking=True)
-        bt_dev.copy_(hbt, non_blocking=True)
-        sl_dev.copy_(hsl, non_blocking=True)
-        call(0)
-        call(1)
-        for i in range(2):
-            hout[i].copy_(d[i]["out"], non_blocking=True)
-            hlse[i].copy_(d[i]["lse"], non_blocking=True)
-        e2e_ev[s][1].record(stream)
-        flush.fill_(float(s & 7))
+        e2e_step(s)
+    stream.wait_stream(copy)                         # the last read-back is inside the region
+    e_end.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in e2e_ev), dist, dev)
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dist, dev)
     e2e_value = job_value(world, step_bytes, e2e_ms / args.steps)
+    # the last step's results reached the host intact: the kernels are
+    # deterministic, so they equal the device-resident loop's (same inputs)
+    last = (args.steps - 1) & 1
+    for i in range(2):
+        assert torch.equal(hov[last][i].view(torch.int16), d[i]["out"].cpu().view(torch.int16))
     assert pkv.check_errors(local_rank) == 0
 
     if dist:
@@ -566,7 +622,9 @@ def run_gpu(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": 64 * world, "seed": args.seed,
                    "kv_bytes_per_step": step_bytes, "kv_bytes_full_layer": kv_bytes[0],
-                   "l2": "flushed between steps (512 MiB write outside the timed events)",
+                   "l2": "flushed between steps (512 MiB write outside the timed events); "
+                         "e2e loop: inputs larger than L2 (777 MB of KV per step), copies "
+                         "double-buffered on a second stream",
                    "parallelism": f"{world} independent ranks" if world > 1 else "single GPU"},
         "calls_per_s": calls_per_s,
         "hbm_frac_of_measured": value / peak,
