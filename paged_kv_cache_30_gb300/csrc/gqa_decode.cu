@@ -555,13 +555,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 template <int P>
 cudaError_t launch_page(const GqaParams& p, const CUtensorMap& kv_map, int grid,
                         cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        gqa_decode_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t e = set_smem_attr_once(gqa_decode_kernel<P>, kSmemBytes, attr_done);
+  if (e != cudaSuccess) return e;
   // launched as a programmatic dependent of the previous kernel on the stream:
   // its launch and shared-memory setup overlap that kernel's tail
   cudaLaunchConfig_t cfg = {};

@@ -632,13 +632,9 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 template <bool kFp8>
 cudaError_t launch_t(const MlaParams& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
                      int grid, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        mla_verify_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kFp8>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t e = set_smem_attr_once(mla_verify_kernel<kFp8>, Cfg<kFp8>::kSmemBytes, attr_done);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(Cfg<kFp8>::kThreads);

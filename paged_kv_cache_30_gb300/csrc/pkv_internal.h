@@ -2,6 +2,8 @@
 // kernel translation units.  Not part of the public ABI.
 #pragma once
 #include <cuda.h>
+
+#include <atomic>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -146,6 +148,20 @@ struct AppendParams {
 };
 cudaError_t launch_gqa_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_mla_kv_append(const AppendParams& p, cudaStream_t stream);
+
+// Large dynamic shared memory is an attribute of a kernel on the current
+// device: set it the first time a kernel launches on each device.
+template <typename Kernel>
+inline cudaError_t set_smem_attr_once(Kernel* fn, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // The counter region of the workspace holds 2^20 ints: the first half for
 // (request, kv head) counters, the second half for split-group counters.
