@@ -109,15 +109,16 @@ __device__ __forceinline__ int clamped_len(const MlaParams& p, int b) {
 // the short requests' CTAs fill the end of the launch.  Every CTA ranks the
 // requests itself (B <= 512; beyond that, request order).
 constexpr int kLptMaxB = 512;
-__device__ __forceinline__ int request_of_rank(const MlaParams& p, int R, int* s_b) {
+__device__ __forceinline__ int request_of_rank(const MlaParams& p, int R, int* s_b, int* s_len) {
   if (p.B > kLptMaxB) return R;
   if (threadIdx.x == 0) *s_b = R;
+  for (int b = threadIdx.x; b < p.B; b += blockDim.x) s_len[b] = clamped_len(p, b);
   __syncthreads();
   for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-    const int Lb = clamped_len(p, b);
+    const int Lb = s_len[b];
     int r = 0;
     for (int b2 = 0; b2 < p.B; ++b2) {
-      const int L2 = clamped_len(p, b2);
+      const int L2 = s_len[b2];
       r += (L2 > Lb) || (L2 == Lb && b2 < b);
     }
     if (r == R) *s_b = b;
@@ -126,7 +127,7 @@ __device__ __forceinline__ int request_of_rank(const MlaParams& p, int R, int* s
   return *s_b;
 }
 
-__device__ __forceinline__ Unit decode_unit(const MlaParams& p, int* s_b) {
+__device__ __forceinline__ Unit decode_unit(const MlaParams& p, int* s_b, int* s_len) {
   Unit u;
   int x = blockIdx.x;
   u.half = x & 1;
@@ -134,7 +135,7 @@ __device__ __forceinline__ Unit decode_unit(const MlaParams& p, int* s_b) {
   u.t = x % p.qlen;
   x /= p.qlen;
   u.split = x % p.cap;
-  u.b = request_of_rank(p, x / p.cap, s_b);
+  u.b = request_of_rank(p, x / p.cap, s_b, s_len);
   int L = __ldg(p.seq_lens + u.b);
   if (L < 0) L = 0;
   if ((long long)L > (long long)p.max_blocks * p.page_size) L = p.max_blocks * p.page_size;
@@ -176,7 +177,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   griddep_wait();
   griddep_launch_dependents();
   __shared__ int s_rank_b;
-  const Unit u = decode_unit(p, &s_rank_b);
+  __shared__ int s_lens[kLptMaxB];
+  const Unit u = decode_unit(p, &s_rank_b, s_lens);
   if (u.split >= u.nsplit) return;  // this request needs fewer splits
 
   extern __shared__ uint8_t smem_raw[];
