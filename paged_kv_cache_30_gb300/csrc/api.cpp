@@ -555,7 +555,8 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
   // splits: at most 16 per (request, token, half); the device uses fewer for
   // short requests (at least 4096 keys per split)
   int64_t cap = num_kv_splits == 0 ? 16 : std::min<int64_t>(num_kv_splits, 16);
-  const int64_t max_slots = int64_t(ws.partial_bytes) / (pkv::kMlaPartialFloats * 4);
+  // each slot: one partial plus one plan entry (the plan sits at the end)
+  const int64_t max_slots = int64_t(ws.partial_bytes) / (pkv::kMlaPartialFloats * 4 + 4);
   const int64_t units = B * qlen * 2;
   if (units > pkv::kTopCounters)
     return fail(PKV_ERR_WORKSPACE, "%lld (row, half) units exceed the counters", (long long)units);
@@ -563,6 +564,15 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
   if (units * cap > max_slots || units * cap >= (int64_t(1) << 31))
     return fail(PKV_ERR_WORKSPACE, "workspace holds %lld MLA partials, %lld needed",
                 (long long)max_slots, (long long)(units * cap));
+  {
+    // no request holds more than max_blocks * page_size keys, so none uses
+    // more splits than that many keys need: fewer CTAs with nothing to do
+    const int64_t max_keys =
+        std::min<int64_t>(block_table->shape[1], int64_t(1) << 30) * int64_t(page_size);
+    const int64_t max_tiles = (max_keys + pkv::kMlaTile - 1) / pkv::kMlaTile;
+    const int64_t need = (max_tiles + pkv::kMlaMinTiles - 1) / pkv::kMlaMinTiles;
+    cap = std::max<int64_t>(1, std::min<int64_t>(cap, need));
+  }
 
   EncodeTiledFn encode = nullptr;
   if ((rc = get_encoder(&encode))) return rc;
@@ -623,6 +633,8 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
   p.partials = ws.partials;
   p.max_slots = max_slots;
   p.counters = ws.counters;
+  p.plan = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws.partials) + ws.partial_bytes) -
+           units * cap;
   p.err = ws.err;
   if ((rc = order_streams(st, stream, capturing))) return rc;
   const cudaError_t e =

@@ -9,8 +9,11 @@
 // ("vllm.v1.attention.ops.triton_decode_attention", decode_attention_fwd_verify:
 // parameters).  An FP8 e4m3 cache is dequantised by the scalar k_scale.
 //
-// One CTA per (request, split, verify token, half of the 512 output dims);
-// inactive splits return at once.  Tensor memory (512 columns) holds the
+// One CTA per unit = (request, split, verify token, half of the 512 output
+// dims).  A one-CTA planning kernel first writes each CTA's unit: requests
+// longest first, a request's units side by side, the CTAs without a unit
+// (the launch is sized for the largest split count) at the end, where they
+// return at once.  Tensor memory (512 columns) holds the
 // CTA's output half O[128 x 256] (fp32), two score buffers S[128 x 32] and
 // query dims [0, 384) as bf16 pairs (the A operand of 24 of the 36 K16 steps
 // of S: an MMA with A in TMEM reads only B from shared memory, and shared
@@ -37,7 +40,8 @@
 //               shared memory; epilogue.
 // The two halves both compute S (576-wide Q K^T) and each does half of P V.
 // Splits of a request publish fp32 (O half, m, l) partials; the last CTA of a
-// (request, token, half) merges them and resets its arrival counter.
+// (request, token, half) merges them with its own O, still in tensor memory,
+// and resets its arrival counter.
 #include "pkv_internal.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -104,41 +108,30 @@ __device__ __forceinline__ int clamped_len(const MlaParams& p, int b) {
   return L;
 }
 
-// Requests are served longest first: CTA block x belongs to the request of
-// rank x / (cap * qlen * 2) in order of decreasing length (ties by index), so
-// the short requests' CTAs fill the end of the launch.  Every CTA ranks the
-// requests itself (B <= 512; beyond that, request order).
-constexpr int kLptMaxB = 512;
-__device__ __forceinline__ int request_of_rank(const MlaParams& p, int R, int* s_b, int* s_len) {
-  if (p.B > kLptMaxB) return R;
-  if (threadIdx.x == 0) *s_b = R;
-  for (int b = threadIdx.x; b < p.B; b += blockDim.x) s_len[b] = clamped_len(p, b);
-  __syncthreads();
-  for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-    const int Lb = s_len[b];
-    int r = 0;
-    for (int b2 = 0; b2 < p.B; ++b2) {
-      const int L2 = s_len[b2];
-      r += (L2 > Lb) || (L2 == Lb && b2 < b);
-    }
-    if (r == R) *s_b = b;
-  }
-  __syncthreads();
-  return *s_b;
+__device__ __forceinline__ int split_count(const MlaParams& p, int L) {
+  const int req_tiles = (L + kMlaTile - 1) / kMlaTile;
+  const int ns = (req_tiles + kMlaMinTiles - 1) / kMlaMinTiles;
+  return ns < 1 ? 1 : (ns > p.cap ? p.cap : ns);
 }
 
-__device__ __forceinline__ Unit decode_unit(const MlaParams& p, int* s_b, int* s_len) {
+// The unit of this CTA, from the plan the planning kernel wrote: entry
+// ((b * qlen + t) * 2 + half) * 16 + split, or -1 (returned as split 0 of
+// nsplit 0: no unit).
+__device__ __forceinline__ Unit decode_unit(const MlaParams& p) {
   Unit u;
-  int x = blockIdx.x;
-  u.half = x & 1;
-  x >>= 1;
-  u.t = x % p.qlen;
-  x /= p.qlen;
-  u.split = x % p.cap;
-  u.b = request_of_rank(p, x / p.cap, s_b, s_len);
-  int L = __ldg(p.seq_lens + u.b);
-  if (L < 0) L = 0;
-  if ((long long)L > (long long)p.max_blocks * p.page_size) L = p.max_blocks * p.page_size;
+  const int v = __ldg(p.plan + blockIdx.x);
+  if (v < 0) {
+    u.split = 0;
+    u.nsplit = 0;
+    return u;
+  }
+  u.split = v & 15;
+  const int ch = v >> 4;
+  u.half = ch & 1;
+  const int rt = ch >> 1;
+  u.b = rt / p.qlen;
+  u.t = rt - u.b * p.qlen;
+  const int L = clamped_len(p, u.b);
   int Lr = p.real_seq_lens ? __ldg(p.real_seq_lens + u.b) : L;
   int lim = L - p.qlen + 1 + u.t;
   if (Lr < lim) lim = Lr;
@@ -146,8 +139,7 @@ __device__ __forceinline__ Unit decode_unit(const MlaParams& p, int* s_b, int* s
   u.L = L;
   u.lim = lim;
   const int req_tiles = (L + kMlaTile - 1) / kMlaTile;
-  int ns = (req_tiles + kMlaMinTiles - 1) / kMlaMinTiles;
-  ns = ns < 1 ? 1 : (ns > p.cap ? p.cap : ns);
+  const int ns = split_count(p, L);
   u.nsplit = ns;
   const int a = (int)((long long)req_tiles * u.split / ns);
   const int e = (int)((long long)req_tiles * (u.split + 1) / ns);
@@ -176,10 +168,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   // as every CTA of this one has started (it waits for this grid the same way).
   griddep_wait();
   griddep_launch_dependents();
-  __shared__ int s_rank_b;
-  __shared__ int s_lens[kLptMaxB];
-  const Unit u = decode_unit(p, &s_rank_b, s_lens);
-  if (u.split >= u.nsplit) return;  // this request needs fewer splits
+  const Unit u = decode_unit(p);
+  if (u.split >= u.nsplit) return;  // no unit for this CTA
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -400,17 +390,22 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       const uint4* qsrc = reinterpret_cast<const uint4*>(
           p.q + ((long long)u.b * p.qlen + u.t) * p.q_sr + (long long)row * p.q_sh);
 #pragma unroll 1
-      for (int j = 0; j < kQtChunks; ++j) {
-        uint32_t v[32];
+      for (int j0 = 0; j0 < kQtChunks; j0 += 3) {  // 24 loads in flight per thread
+        uint4 w[24];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 w = __ldg(qsrc + 8 * j + k);
-          v[4 * k] = w.x;
-          v[4 * k + 1] = w.y;
-          v[4 * k + 2] = w.z;
-          v[4 * k + 3] = w.w;
+        for (int k = 0; k < 24; ++k) w[k] = __ldg(qsrc + 8 * j0 + k);
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          uint32_t v[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            v[4 * k] = w[8 * j + k].x;
+            v[4 * k + 1] = w[8 * j + k].y;
+            v[4 * k + 2] = w[8 * j + k].z;
+            v[4 * k + 3] = w[8 * j + k].w;
+          }
+          tc::st_32x32b_x32(tmem + lane_base + kTmemQ + 32 * (j0 + j), v);
         }
-        tc::st_32x32b_x32(tmem + lane_base + kTmemQ + 32 * j, v);
       }
       tc::wait_st();
       tc::fence_before_sync();
@@ -530,9 +525,10 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       if (u.half == 0)
         p.lse[r * p.lse_sr + row * p.lse_sh] = (l > 0.f) ? m_used * scale_eff + logf(l) : -INFINITY;
     } else {
-      // publish the split's partial: O half (fp32), m, l
+      // publish the split's partial: O half (fp32, as [64 dim quads][128 heads][4]:
+      // a warp's float4 stores cover 512 contiguous bytes), m, l
       const long long slot = slot_of(p, u, u.split);
-      float* po = p.partials + slot * kMlaPartialFloats + (long long)row * kMlaHalf;
+      float* po = p.partials + slot * kMlaPartialFloats + 4 * row;
       for (int j = 0; j < kMlaHalf / 32; ++j) {
         uint32_t o[32];
         if (n > 0) {
@@ -541,7 +537,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         }
 #pragma unroll
         for (int c = 0; c < 32; c += 4)
-          *reinterpret_cast<float4*>(po + 32 * j + c) =
+          *reinterpret_cast<float4*>(po + (8 * j + c / 4) * (4 * kMlaHeads)) =
               n > 0 ? make_float4(__uint_as_float(o[c]), __uint_as_float(o[c + 1]),
                                   __uint_as_float(o[c + 2]), __uint_as_float(o[c + 3]))
                     : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -563,11 +559,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         float ms_[16], ls_[16];
 #pragma unroll
         for (int s = 0; s < 16; ++s) {
-          if (s < ns) {
+          if (s < ns && s != u.split) {
             const float* ml =
                 p.partials + slot_of(p, u, s) * kMlaPartialFloats + kMlaHeads * kMlaHalf;
             ms_[s] = __ldcg(ml + row);
             ls_[s] = __ldcg(ml + kMlaHeads + row);
+          } else {  // this split's own (m, l); its O is still in tensor memory
+            ms_[s] = m_used;
+            ls_[s] = l;
           }
         }
         float M = -INFINITY;
@@ -585,17 +584,29 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           }
         }
         const float inv = (Ls > 0.f) ? out_scale / Ls : 0.f;
+        float w_own = 0.f;
+#pragma unroll
+        for (int s = 0; s < 16; ++s)
+          if (s == u.split) w_own = w[s];
         for (int j = 0; j < kMlaHalf; j += 32) {
           float acc[32];
+          {
+            uint32_t o[32];
+            if (n > 0) {
+              tc::ld_32x32b_x32(tmem + lane_base + kTmemO + j, o);
+              tc::wait_ld();
+            }
 #pragma unroll
-          for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+            for (int e = 0; e < 32; ++e) acc[e] = n > 0 ? w_own * __uint_as_float(o[e]) : 0.f;
+          }
 #pragma unroll 4
           for (int s = 0; s < ns; ++s) {
+            if (s == u.split) continue;
             const float* src =
-                p.partials + slot_of(p, u, s) * kMlaPartialFloats + (long long)row * kMlaHalf + j;
+                p.partials + slot_of(p, u, s) * kMlaPartialFloats + 4 * row + (j / 4) * (4 * kMlaHeads);
             float4 v[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = ldcg_f4(src + 4 * k);
+            for (int k = 0; k < 8; ++k) v[k] = ldcg_f4(src + k * (4 * kMlaHeads));
             const float ws = w[s];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -631,23 +642,125 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   }
 }
 
-template <bool kFp8>
-cudaError_t launch_t(const MlaParams& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
-                     int grid, cudaStream_t stream) {
-  static std::atomic<uint64_t> attr_done{0};
-  const cudaError_t e = set_smem_attr_once(mla_verify_kernel<kFp8>, Cfg<kFp8>::kSmemBytes, attr_done);
-  if (e != cudaSuccess) return e;
+// ------------------------------------------------------------ work plan --
+// One CTA writes every verify CTA's unit (see decode_unit) or -1: the units
+// with split < the request's split count, requests in order of decreasing
+// length (ties by request index; beyond kPlanSortMax requests, request order),
+// a request's units consecutive (split-major, then verify token, then half:
+// the CTAs that read the same keys run side by side), then -1 to the end.
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanSortMax = 8192;
+
+__global__ void __launch_bounds__(kPlanThreads, 1)
+    mla_plan_kernel(const __grid_constant__ MlaParams p, int grid) {
+  griddep_wait();
+  griddep_launch_dependents();
+  extern __shared__ unsigned long long keys[];  // [P2] (length, request) sort keys
+  __shared__ int warp_sums[kPlanThreads / 32];
+  __shared__ int s_total;
+  const int B = p.B, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int per_split = p.qlen * 2;
+  auto entry = [&](int b, int split, int t, int half) {
+    return (((b * p.qlen + t) * 2 + half) << 4) | split;
+  };
+  if (B > kPlanSortMax) {  // request order, a fixed slot per (request, split)
+    for (int x = tid; x < grid; x += kPlanThreads) {
+      const int per_b = p.cap * per_split;
+      const int b = x / per_b, rem = x - b * per_b;
+      const int split = rem / per_split, th = rem - split * per_split;
+      p.plan[x] = split < split_count(p, clamped_len(p, b)) ? entry(b, split, th >> 1, th & 1) : -1;
+    }
+    return;
+  }
+  int P2 = 1;
+  while (P2 < B) P2 <<= 1;
+  for (int i = tid; i < P2; i += kPlanThreads) {
+    unsigned long long k = ~0ull;
+    if (i < B)
+      k = ((unsigned long long)(0x7fffffff - clamped_len(p, i)) << 32) | (unsigned)i;
+    keys[i] = k;
+  }
+  __syncthreads();
+  for (int k = 2; k <= P2; k <<= 1)  // bitonic sort, ascending
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < P2; i += kPlanThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long x0 = keys[i], x1 = keys[ixj];
+          if ((x0 > x1) == ((i & k) == 0)) {
+            keys[i] = x1;
+            keys[ixj] = x0;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  // ranks [r0, r0 + R) of this thread; exclusive scan of their unit counts
+  const int R = (B + kPlanThreads - 1) / kPlanThreads;
+  const int r0 = min(B, tid * R), r1 = min(B, r0 + R);
+  int mine = 0;
+  for (int r = r0; r < r1; ++r)
+    mine += split_count(p, 0x7fffffff - (int)(keys[r] >> 32)) * per_split;
+  int incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  if (lane == 31) warp_sums[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int v = warp_sums[lane];
+    int wi = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += t;
+    }
+    warp_sums[lane] = wi - v;
+    if (lane == 31) s_total = wi;
+  }
+  __syncthreads();
+  int x = warp_sums[wid] + incl - mine;
+  for (int r = r0; r < r1; ++r) {
+    const int L = 0x7fffffff - (int)(keys[r] >> 32), b = (int)(keys[r] & 0xffffffffu);
+    const int ns = split_count(p, L);
+    for (int split = 0; split < ns; ++split)
+      for (int th = 0; th < per_split; ++th) p.plan[x++] = entry(b, split, th >> 1, th & 1);
+  }
+  for (int y = s_total + tid; y < grid; y += kPlanThreads) p.plan[y] = -1;
+}
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel* fn, int grid, int threads, int smem, cudaStream_t stream,
+                       Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(Cfg<kFp8>::kThreads);
-  cfg.dynamicSmemBytes = Cfg<kFp8>::kSmemBytes;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_verify_kernel<kFp8>, p, q_map, kv_map);
+  return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
+template <bool kFp8>
+cudaError_t launch_t(const MlaParams& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
+                     int grid, cudaStream_t stream) {
+  static std::atomic<uint64_t> attr_done{0}, plan_attr_done{0};
+  cudaError_t e = set_smem_attr_once(mla_verify_kernel<kFp8>, Cfg<kFp8>::kSmemBytes, attr_done);
+  if (e != cudaSuccess) return e;
+  e = set_smem_attr_once(mla_plan_kernel, kPlanSortMax * 8, plan_attr_done);
+  if (e != cudaSuccess) return e;
+  int p2 = 1;
+  while (p2 < p.B) p2 <<= 1;
+  e = launch_pdl(mla_plan_kernel, 1, kPlanThreads, p.B > kPlanSortMax ? 0 : p2 * 8, stream, p, grid);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(mla_verify_kernel<kFp8>, grid, Cfg<kFp8>::kThreads, Cfg<kFp8>::kSmemBytes,
+                    stream, p, q_map, kv_map);
 }
 
 }  // namespace

@@ -123,6 +123,7 @@ struct MlaParams {
   float* partials;               // [slots][128*256 + 256]
   int64_t max_slots;
   int* counters;                 // [(b*qlen + t)*2 + half]
+  int* plan;                     // [grid] unit of each CTA (written by the planning kernel)
   int* err;
 };
 
