@@ -10,8 +10,8 @@
 // parameters).  An FP8 e4m3 cache is dequantised by the scalar k_scale.
 //
 // One CTA per unit = (request, split, verify token, half of the 512 output
-// dims).  A one-CTA planning kernel first writes each CTA's unit: requests
-// longest first, a request's units side by side, the CTAs without a unit
+// dims).  A one-CTA planning kernel first writes each CTA's unit: largest
+// splits first, a request's units side by side, the CTAs without a unit
 // (the launch is sized for the largest split count) at the end, where they
 // return at once.  Tensor memory (512 columns) holds the
 // CTA's output half O[128 x 256] (fp32), two score buffers S[128 x 32] and
@@ -33,11 +33,14 @@
 //               K16 steps with A from TMEM, 12 with A from shared memory) and
 //               O += P V (M 128, N 256, K 32; P K-major with 64-byte swizzle,
 //               V = the same smem tile read MN-major).
-//   warps 4..7  query dims [0, 384) into TMEM, then softmax, one thread per
+//   warps 4..7  softmax, one thread per
 //               head: S from TMEM, mask j >= lim, exp2-domain online softmax
 //               with a lazily updated max (O in TMEM is rescaled only when
 //               the max grows by more than 2^8), P rounded to bf16 into
 //               shared memory; epilogue.
+// Warps 0..7 first share the load of query dims [0, 384) into TMEM (one
+// round of 16-byte loads per thread; the producer's share comes after it has
+// issued the ring's first fill).
 // The two halves both compute S (576-wide Q K^T) and each does half of P V.
 // Splits of a request publish fp32 (O half, m, l) partials; the last CTA of a
 // (request, token, half) merges them with its own O, still in tensor memory,
@@ -114,6 +117,13 @@ __device__ __forceinline__ int split_count(const MlaParams& p, int L) {
   return ns < 1 ? 1 : (ns > p.cap ? p.cap : ns);
 }
 
+// Tiles of the largest split of a request of L keys.
+__device__ __forceinline__ int split_tiles(const MlaParams& p, int L) {
+  const int req_tiles = (L + kMlaTile - 1) / kMlaTile;
+  const int ns = split_count(p, L);
+  return (req_tiles + ns - 1) / ns;
+}
+
 // The unit of this CTA, from the plan the planning kernel wrote: entry
 // ((b * qlen + t) * 2 + half) * 16 + split, or -1 (returned as split 0 of
 // nsplit 0: no unit).
@@ -187,7 +197,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   static_assert(C::kStages <= kMaxStages && C::kF8Stages <= kMaxStages, "barrier slots");
   if (tid == 0) {
     mbar_init(bar(kQFull), 1);
-    mbar_init(bar(kQtReady), 128);
+    mbar_init(bar(kQtReady), 256);
     for (int s = 0; s < kMaxStages; ++s) {  // every barrier either path may touch
       mbar_init(bar(kKvFull + s), 1);
       mbar_init(bar(kKvEmpty + s), 1);
@@ -218,6 +228,34 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
   const float c2 = scale_eff * kLog2e;
   const int n = u.ntiles;
 
+  // Query dims [0, 384) into TMEM (the A operand of the first 24 K16 steps of
+  // S = Q K^T), shared by warps 0..7: warp w writes TMEM lanes (heads)
+  // 32 (w % 4) .. + 31, 64-dim chunks 3 (w / 4) .. + 2, one round of 24
+  // 16-byte loads per thread; 256 arrivals on kQtReady.
+  auto load_qt_share = [&]() {
+    const int head = 32 * (warp & 3) + lane, c0 = 3 * ((warp >> 2) & 1);
+    const uint4* qsrc = reinterpret_cast<const uint4*>(
+        p.q + ((long long)u.b * p.qlen + u.t) * p.q_sr + (long long)head * p.q_sh) + 8 * c0;
+    uint4 w[24];
+#pragma unroll
+    for (int k = 0; k < 24; ++k) w[k] = __ldg(qsrc + k);
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      uint32_t v[32];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        v[4 * k] = w[8 * j + k].x;
+        v[4 * k + 1] = w[8 * j + k].y;
+        v[4 * k + 2] = w[8 * j + k].z;
+        v[4 * k + 3] = w[8 * j + k].w;
+      }
+      tc::st_32x32b_x32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kTmemQ + 32 * (c0 + j), v);
+    }
+    tc::wait_st();
+    tc::fence_before_sync();
+    mbar_arrive(bar(kQtReady));
+  };
+
   if (warp == 0) {
     // ============================ TMA producer ============================
     if (n > 0) {
@@ -246,6 +284,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         int blk, off;
         piece(g, blk, off);
         for (int i = g; i < min(n, g + 16); ++i) {
+          // the ring's first fill needs no wait: the query share comes after it
+          if (i == min(n, kFp8 ? C::kF8Ring : kStages)) load_qt_share();
           const int b0 = __shfl_sync(0xffffffffu, blk, 2 * (i - g));
           const int o0 = __shfl_sync(0xffffffffu, off, 2 * (i - g));
           const int b1 = __shfl_sync(0xffffffffu, blk, 2 * (i - g) + 1);
@@ -275,12 +315,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           }
         }
       }
+      if (n <= (kFp8 ? C::kF8Ring : kStages)) load_qt_share();
     }
   } else if (warp == 1) {
     // ============================= MMA issuer =============================
     if (n > 0) {
       const uint32_t id_s = tc::idesc_bf16_f32(128, kMlaTile, false, false);
       const uint32_t id_pv = tc::idesc_bf16_f32(128, kMlaHalf, false, true);
+      load_qt_share();
       mbar_wait(bar(kQFull), 0, p.err);
       mbar_wait(bar(kQtReady), 0, p.err);
       auto do_pv = [&](int j) {
@@ -329,11 +371,14 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
       }
       do_pv(n - 1);
     }
+  } else if (!kFp8 && (warp == 2 || warp == 3)) {
+    if (n > 0) load_qt_share();
   } else if (kFp8 && (warp == 2 || warp == 3 || warp >= 8)) {
     // ============ FP8: e4m3 tile -> bf16 tile in the MMA's swizzled layout ============
     // Exact: every e4m3 value is a bf16 value.  k_scale is applied to the scores
     // and to the output instead.
     const int ct = (warp < 8) ? tid - 64 : tid - 256 + 64;  // 0 .. 191
+    if (warp < 8 && n > 0) load_qt_share();
     for (int i = 0; i < n; ++i) {
       const int sf = i % C::kF8Ring, st = i % kStages;
       mbar_wait(bar(kF8Full + sf), (i / C::kF8Ring) & 1, p.err);
@@ -385,31 +430,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     uint8_t* p_row = base + C::kOffP + (row / 8) * 512 + (row % 8) * 64;
     const int pswz = (row % 8) >> 1;
     if (n > 0) {
-      // query dims [0, 384) of this head into TMEM lane `row`: the A operand
-      // of the first 24 K16 steps of S = Q K^T
-      const uint4* qsrc = reinterpret_cast<const uint4*>(
-          p.q + ((long long)u.b * p.qlen + u.t) * p.q_sr + (long long)row * p.q_sh);
-#pragma unroll 1
-      for (int j0 = 0; j0 < kQtChunks; j0 += 3) {  // 24 loads in flight per thread
-        uint4 w[24];
-#pragma unroll
-        for (int k = 0; k < 24; ++k) w[k] = __ldg(qsrc + 8 * j0 + k);
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          uint32_t v[32];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            v[4 * k] = w[8 * j + k].x;
-            v[4 * k + 1] = w[8 * j + k].y;
-            v[4 * k + 2] = w[8 * j + k].z;
-            v[4 * k + 3] = w[8 * j + k].w;
-          }
-          tc::st_32x32b_x32(tmem + lane_base + kTmemQ + 32 * (j0 + j), v);
-        }
-      }
-      tc::wait_st();
-      tc::fence_before_sync();
-      mbar_arrive(bar(kQtReady));
+      load_qt_share();
     }
     for (int i = 0; i < n; ++i) {
       const int sb = i & 1;
@@ -584,29 +605,30 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           }
         }
         const float inv = (Ls > 0.f) ? out_scale / Ls : 0.f;
-        float w_own = 0.f;
-#pragma unroll
-        for (int s = 0; s < 16; ++s)
-          if (s == u.split) w_own = w[s];
         for (int j = 0; j < kMlaHalf; j += 32) {
           float acc[32];
-          {
-            uint32_t o[32];
-            if (n > 0) {
-              tc::ld_32x32b_x32(tmem + lane_base + kTmemO + j, o);
-              tc::wait_ld();
-            }
 #pragma unroll
-            for (int e = 0; e < 32; ++e) acc[e] = n > 0 ? w_own * __uint_as_float(o[e]) : 0.f;
-          }
+          for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+          // splits in index order, whichever of them merges (the result is the
+          // same bits every call); this split's own O comes from tensor memory
 #pragma unroll 4
           for (int s = 0; s < ns; ++s) {
-            if (s == u.split) continue;
-            const float* src =
-                p.partials + slot_of(p, u, s) * kMlaPartialFloats + 4 * row + (j / 4) * (4 * kMlaHeads);
             float4 v[8];
+            if (s == u.split) {
+              uint32_t o[32];
+              tc::ld_32x32b_x32(tmem + lane_base + kTmemO + j, o);
+              tc::wait_ld();
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = ldcg_f4(src + k * (4 * kMlaHeads));
+              for (int k = 0; k < 8; ++k)
+                v[k] = n > 0 ? make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                           __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+              const float* src = p.partials + slot_of(p, u, s) * kMlaPartialFloats + 4 * row +
+                                 (j / 4) * (4 * kMlaHeads);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) v[k] = ldcg_f4(src + k * (4 * kMlaHeads));
+            }
             const float ws = w[s];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -643,11 +665,13 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 }
 
 // ------------------------------------------------------------ work plan --
-// One CTA writes every verify CTA's unit (see decode_unit) or -1: the units
-// with split < the request's split count, requests in order of decreasing
-// length (ties by request index; beyond kPlanSortMax requests, request order),
-// a request's units consecutive (split-major, then verify token, then half:
-// the CTAs that read the same keys run side by side), then -1 to the end.
+// One CTA writes every verify CTA's unit (see decode_unit) or -1.  The
+// units (split < the request's split count) come in order of decreasing
+// split size, i.e. tiles per split, ties by request index (beyond
+// kPlanSortMax requests: request order), so the CTAs that start last are the
+// short ones; a request's units are consecutive (split-major, then verify
+// token, then half: the CTAs that read the same keys run side by side); -1
+// fills the rest of the launch.
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanSortMax = 8192;
 
@@ -677,7 +701,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   for (int i = tid; i < P2; i += kPlanThreads) {
     unsigned long long k = ~0ull;
     if (i < B)
-      k = ((unsigned long long)(0x7fffffff - clamped_len(p, i)) << 32) | (unsigned)i;
+      k = ((unsigned long long)(0x7fffffff - split_tiles(p, clamped_len(p, i))) << 32) | (unsigned)i;
     keys[i] = k;
   }
   __syncthreads();
@@ -700,7 +724,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   const int r0 = min(B, tid * R), r1 = min(B, r0 + R);
   int mine = 0;
   for (int r = r0; r < r1; ++r)
-    mine += split_count(p, 0x7fffffff - (int)(keys[r] >> 32)) * per_split;
+    mine += split_count(p, clamped_len(p, (int)(keys[r] & 0xffffffffu))) * per_split;
   int incl = mine;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -723,8 +747,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   __syncthreads();
   int x = warp_sums[wid] + incl - mine;
   for (int r = r0; r < r1; ++r) {
-    const int L = 0x7fffffff - (int)(keys[r] >> 32), b = (int)(keys[r] & 0xffffffffu);
-    const int ns = split_count(p, L);
+    const int b = (int)(keys[r] & 0xffffffffu);
+    const int ns = split_count(p, clamped_len(p, b));
     for (int split = 0; split < ns; ++split)
       for (int th = 0; th < per_split; ++th) p.plan[x++] = entry(b, split, th >> 1, th & 1);
   }
