@@ -453,7 +453,12 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
   p.min_pages = 256 / page_size;  // a split streams at least 256 tokens (128 KB per kv head)
   const int64_t grid64 = std::min<int64_t>(int64_t(ws.num_sms) * pkv::gqa_ctas_per_sm(), bh * cap);
   const int grid = int(grid64 < 1 ? 1 : grid64);
-  p.target_items = grid * 4;  // about four items per CTA (A/B on GB300: best of 2..24)
+  // About four items per CTA (A/B on the Flint batch: best of 2..24), but no
+  // more than 16 per (request, kv head) while that still gives every CTA one:
+  // a few long requests then stream fewer, larger splits, each merged in a
+  // single 16-way level (one 131072-token request, auto cap, on GB300:
+  // 118.7 -> 106.5 us; eight of them 632.8 -> 627.4 us).
+  p.target_items = int(std::max<int64_t>(grid, std::min<int64_t>(int64_t(grid) * 4, bh * 16)));
   p.part_o = ws.partials;
   p.part_ml = ws.partials + max_items * pkv::kGqaPartialFloats;
   p.max_items = max_items;
