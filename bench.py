@@ -167,7 +167,9 @@ def make_layers(seed: int):
 
 def oracle_baseline(layers, budget_s: float, threads: int):
     """Time the fp64 oracle on a bounded sample: whole (request, kv head)
-    groups of the full layer, taken round-robin, until ~budget_s of work."""
+    groups of the full layer, longest requests first, round-robin over the
+    layer (again from the start once every group is done), until ~budget_s of
+    work."""
     import numpy as np
     import oracle
     full = layers[0]
@@ -177,7 +179,7 @@ def oracle_baseline(layers, budget_s: float, threads: int):
     order = np.argsort(-L)  # longest first: representative bytes per second
     done_bytes, t_used, groups = 0, 0.0, 0
     i = 0
-    while t_used < budget_s and i < B * Hkv:
+    while t_used < budget_s:
         b = int(order[(i // Hkv) % B])
         kvh = i % Hkv
         rows = np.arange(b * Hq + kvh * 8, b * Hq + kvh * 8 + 8, dtype=np.int64)
@@ -608,8 +610,10 @@ def run_gpu(args, rank, world, local_rank):
         v, t_used, groups = oracle_baseline(layers, args.cpu_budget, threads)
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{groups} (request, kv head) groups of the full-attention layer "
-                         f"(longest requests first, all 8 query heads each), "
-                         f"{t_used:.1f} s of fp64 oracle work on {threads} threads"}
+                         f"(longest requests first, all 8 query heads each, "
+                         f"{groups / (layers[0].q.shape[0] * layers[0].kv_cache.shape[1]):.1f} "
+                         f"passes over the layer), {t_used:.1f} s of fp64 oracle work on "
+                         f"{threads} threads"}
 
     extra = None
     if world == 1 and not args.no_extra:

@@ -180,3 +180,28 @@ def test_mla_request_order_paths():
         L = rng.choice([1, 17, 33, 40], size=B).astype(np.int32)
         prob = mla_case(seed, L, 1, 16, has_real=False, cap=2)
         check(prob, what=f"mla order B={B}")
+
+
+def test_mla_plan_beyond_sort_limit():
+    """8200 requests, above the planning kernel's 8192-request sort: units in
+    request order with a fixed CTA slot per (request, split), most slots idle;
+    six requests long enough for two splits.  A larger workspace holds the
+    16400 x 2 partial slots.  Sampled rows (and rows of every long request)
+    against the oracle."""
+    rng = np.random.default_rng(21)
+    B = 8200
+    L = rng.choice([1, 17, 33, 40], size=B).astype(np.int32)
+    long_idx = rng.choice(B, size=6, replace=False)
+    L[long_idx] = [4100, 5000, 4097, 4500, 6000, 4200]
+    prob = W.mla_problem(21, B=B, qlen=1, H=128, page_size=16, lengths="const", Lmin=1,
+                         Lmax=int(L.max()), seq_lens=L, has_real=False, num_kv_splits=2)
+    rows = np.concatenate([rng.choice(B * 128, size=512, replace=False),
+                           (long_idx[:, None] * 128 + np.arange(0, 128, 16)).ravel()])
+    pkv.shutdown()
+    try:
+        pkv.init(0, 6 << 30)
+        check(prob, rows=rows, what="mla plan B=8200")
+        assert pkv.check_counters(0) == 0
+    finally:
+        pkv.shutdown()
+        pkv.init(0)
