@@ -72,6 +72,17 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         i32, i32, i32, i32,      # B, H, Lk, Lv
         vp, i64, vp, vp, i32]    # rows, nrows, out, lse, nthreads
     lib.pkv_oracle_mla_verify.restype = i32
+    lib.pkv_oracle_mla_verify_q8.argtypes = [
+        vp, i64, i64, vp, i64,   # q8 codes, strides, q scales, row stride
+        vp, i32, i64, i64, i64,  # cache, fp8, strides, num_pages
+        vp, i64, i64,            # block table, stride, max_blocks
+        vp, vp,                  # seq_lens, real_seq_lens
+        i32, dbl, i32, dbl,      # qlen, scale, page_size, k_scale
+        i32, i32, i32, i32,      # B, H, Lk, Lv
+        vp, i64, vp, vp, i32]    # rows, nrows, out, lse, nthreads
+    lib.pkv_oracle_mla_verify_q8.restype = i32
+    lib.pkv_oracle_mla_quantize_q.argtypes = [vp, i64, i64, i32, i32, i32, vp, vp]
+    lib.pkv_oracle_mla_quantize_q.restype = i32
     lib.pkv_oracle_f32_to_e4m3.restype = ctypes.c_uint8
     lib.pkv_oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
     i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
@@ -204,6 +215,59 @@ def mla_verify(q, latent_cache, block_table, seq_lens, real_seq_lens, qlen, scal
         _ptr(rws), nrows, _ptr(out), _ptr(lse), _threads(nthreads))
     if rc != 0:
         raise OracleError(f"pkv_oracle_mla_verify failed with status {rc}")
+    return out, lse
+
+
+def mla_quantize_q(q, lib=None):
+    """Per-(row, head) e4m3 quantisation of an MLA query [R, H, Lk] bf16:
+    scale = absmax / 448 (fp32), code = e4m3(q / scale) with the quotient in
+    fp32.  Returns (codes uint8 [R, H, Lk], scales float32 [R, H])."""
+    lib = lib or load()
+    qn = _np(q, np.uint16)
+    R, H, Lk = qn.shape
+    codes = np.zeros((R, H, Lk), dtype=np.uint8)
+    scales = np.zeros((R, H), dtype=np.float32)
+    rc = lib.pkv_oracle_mla_quantize_q(_ptr(qn), H * Lk, Lk, R, H, Lk, _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise OracleError(f"pkv_oracle_mla_quantize_q failed with status {rc}")
+    return codes, scales
+
+
+def mla_verify_q8(q8, q_scale, latent_cache, block_table, seq_lens, real_seq_lens, qlen, scale,
+                  page_size, k_scale=None, Lv=512, rows=None, nthreads=None, lib=None):
+    """mla_verify with the query given as e4m3 codes [B*qlen, H, Lk] (uint8)
+    and per-(row, head) fp32 scales [B*qlen, H]: query = code value x scale."""
+    import torch
+    lib = lib or load()
+    fp8 = int(latent_cache.dtype == torch.float8_e4m3fn)
+    qn = np.ascontiguousarray(np.asarray(q8, dtype=np.uint8))
+    qs = np.ascontiguousarray(np.asarray(q_scale, dtype=np.float32))
+    cn = _np(latent_cache, np.uint8 if fp8 else np.uint16)
+    btn = _np(block_table, np.int32)
+    sln = _np(seq_lens, np.int32)
+    rln = _np(real_seq_lens, np.int32)
+    R, H, Lk = qn.shape
+    assert R % qlen == 0 and qs.shape == (R, H)
+    B = R // qlen
+    if cn.ndim == 3:
+        cn = cn.reshape(-1, page_size, 1, Lk)
+    num_pages, P, one, Lk2 = cn.shape
+    assert one == 1 and Lk2 == Lk and P == page_size
+    rws = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    nrows = R * H if rws is None else rws.shape[0]
+    out = np.zeros((nrows, Lv), dtype=np.float64)
+    lse = np.zeros((nrows,), dtype=np.float64)
+    ks = 1.0 if (k_scale is None or not fp8) else float(np.float32(k_scale))
+    rc = lib.pkv_oracle_mla_verify_q8(
+        _ptr(qn), H * Lk, Lk, _ptr(qs), H,
+        _ptr(cn), fp8, P * Lk, Lk, num_pages,
+        _ptr(btn), btn.shape[1], btn.shape[1],
+        _ptr(sln), _ptr(rln),
+        int(qlen), float(np.float32(scale)), int(page_size), ks,
+        B, H, Lk, Lv,
+        _ptr(rws), nrows, _ptr(out), _ptr(lse), _threads(nthreads))
+    if rc != 0:
+        raise OracleError(f"pkv_oracle_mla_verify_q8 failed with status {rc}")
     return out, lse
 
 

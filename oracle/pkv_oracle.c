@@ -169,6 +169,9 @@ typedef struct {
     int64_t q_sr, q_sh; /* strides of q [B*qlen, H, Lk] */
     const uint8_t *cache; /* bf16 (2 bytes) or e4m3 (1 byte) elements */
     int fp8;
+    const uint8_t *q8;       /* or: e4m3 query codes [r, h, Lk] (q ignored) */
+    const float *q8_scale;   /* [r, h]: the query is code value * scale */
+    int64_t q8_sr, q8_sh, qs_sr;
     int64_t c_spage, c_stok; /* element strides of the cache [num_pages, P, 1, Lk] */
     int64_t num_pages;
     const int32_t *bt;
@@ -218,8 +221,14 @@ static int mla_row(const mla_job *a, int64_t row, double *out, double *lse) {
         free(x); free(qd); free(kbase);
         return ORACLE_ERR_NOMEM;
     }
-    const uint16_t *qrow = a->q + r * a->q_sr + (int64_t)h * a->q_sh;
-    for (int d = 0; d < Lk; ++d) qd[d] = pkv_oracle_bf16_to_f64(qrow[d]);
+    if (a->q8) {
+        const uint8_t *c8 = a->q8 + r * a->q8_sr + (int64_t)h * a->q8_sh;
+        const double sq = (double)a->q8_scale[r * a->qs_sr + h];
+        for (int d = 0; d < Lk; ++d) qd[d] = pkv_oracle_e4m3_to_f64(c8[d]) * sq;
+    } else {
+        const uint16_t *qrow = a->q + r * a->q_sr + (int64_t)h * a->q_sh;
+        for (int d = 0; d < Lk; ++d) qd[d] = pkv_oracle_bf16_to_f64(qrow[d]);
+    }
     for (int j = 0; j < lim; ++j) {
         const int32_t page = a->bt[(int64_t)b * a->bt_sb + j / P];
         if (page < 0 || (int64_t)page >= a->num_pages) {
@@ -336,9 +345,33 @@ int pkv_oracle_mla_verify(const uint16_t *q, int64_t q_sr, int64_t q_sh,
     if (!rows) nrows = (int64_t)B * qlen * H;
     for (int64_t i = 0; rows && i < nrows; ++i)
         if (rows[i] < 0 || rows[i] >= (int64_t)B * qlen * H) return ORACLE_ERR_ARG;
-    mla_job a = {q, q_sr, q_sh, (const uint8_t *)cache, fp8, c_spage, c_stok, num_pages,
-                 bt, bt_sb, max_blocks, seq_lens, real_seq_lens, qlen, scale, k_scale,
-                 page_size, B, H, Lk, Lv, rows, nrows, out, lse, ORACLE_OK};
+    mla_job a = {q, q_sr, q_sh, (const uint8_t *)cache, fp8, NULL, NULL, 0, 0, 0, c_spage,
+                 c_stok, num_pages, bt, bt_sb, max_blocks, seq_lens, real_seq_lens, qlen, scale,
+                 k_scale, page_size, B, H, Lk, Lv, rows, nrows, out, lse, ORACLE_OK};
+    return run_pool(&a, 1, nthreads);
+}
+
+/* MLA verify with an e4m3-quantised query (see pkv_oracle_mla_quantize_q):
+ * the query of (row r, head h) is code value x q_scale[r, h], exactly, and
+ * everything else is pkv_oracle_mla_verify. */
+int pkv_oracle_mla_verify_q8(const uint8_t *q8, int64_t q8_sr, int64_t q8_sh,
+                             const float *q_scale, int64_t qs_sr, const void *cache, int fp8,
+                             int64_t c_spage, int64_t c_stok, int64_t num_pages,
+                             const int32_t *bt, int64_t bt_sb, int64_t max_blocks,
+                             const int32_t *seq_lens, const int32_t *real_seq_lens, int qlen,
+                             double scale, int page_size, double k_scale, int B, int H, int Lk,
+                             int Lv, const int64_t *rows, int64_t nrows, double *out,
+                             double *lse, int nthreads) {
+    if (!q8 || !q_scale || !cache || !bt || !seq_lens || !out || !lse) return ORACLE_ERR_ARG;
+    if (B < 0 || H <= 0 || qlen <= 0 || Lk <= 0 || Lv <= 0 || Lv > Lk || page_size <= 0)
+        return ORACLE_ERR_ARG;
+    if (!rows) nrows = (int64_t)B * qlen * H;
+    for (int64_t i = 0; rows && i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= (int64_t)B * qlen * H) return ORACLE_ERR_ARG;
+    mla_job a = {NULL, 0, 0, (const uint8_t *)cache, fp8, q8, q_scale, q8_sr, q8_sh, qs_sr,
+                 c_spage, c_stok, num_pages, bt, bt_sb, max_blocks, seq_lens, real_seq_lens,
+                 qlen, scale, k_scale, page_size, B, H, Lk, Lv, rows, nrows, out, lse,
+                 ORACLE_OK};
     return run_pool(&a, 1, nthreads);
 }
 
@@ -397,6 +430,34 @@ uint8_t pkv_oracle_f32_to_e4m3(float x) {
         code = ((E + 7) << 3) | ((int)q - 8);
     }
     return (uint8_t)(code | (s << 7));
+}
+
+/* Query quantisation for the native-FP8 MLA path (a reading of the "Native-FP8
+ * MLA MMA" step: the pages give no recipe): per (row, head), with the absolute
+ * maximum a of the Lk bf16 elements, the scale is s = a / 448 computed in fp32
+ * (round to nearest even; s = 1 when a = 0) and element d is stored as the
+ * e4m3 code of q_d / s, the quotient computed in fp32 (the precision the
+ * library computes it in), rounded as pkv_oracle_f32_to_e4m3 does.  The
+ * dequantised query is code value x s. */
+int pkv_oracle_mla_quantize_q(const uint16_t *q, int64_t q_sr, int64_t q_sh, int R, int H,
+                              int Lk, uint8_t *codes, float *scales) {
+    if (!q || !codes || !scales || R < 0 || H <= 0 || Lk <= 0) return ORACLE_ERR_ARG;
+    for (int64_t r = 0; r < R; ++r)
+        for (int h = 0; h < H; ++h) {
+            const uint16_t *row = q + r * q_sr + (int64_t)h * q_sh;
+            float amax = 0.0f;
+            for (int d = 0; d < Lk; ++d) {
+                const float v = (float)fabs(pkv_oracle_bf16_to_f64(row[d]));
+                if (v > amax) amax = v;
+            }
+            const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+            scales[r * H + h] = sc;
+            for (int d = 0; d < Lk; ++d) {
+                const float x = (float)pkv_oracle_bf16_to_f64(row[d]) / sc;
+                codes[(r * H + h) * (int64_t)Lk + d] = pkv_oracle_f32_to_e4m3(x);
+            }
+        }
+    return ORACLE_OK;
 }
 
 static int append_slot(const int32_t *bt, int64_t bt_sb, int64_t max_blocks, int64_t num_blocks,

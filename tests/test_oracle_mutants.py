@@ -191,3 +191,52 @@ def test_append_mutant_is_caught(name, monkeypatch):
             except (AssertionError, oracle.OracleError):
                 caught.append(fn.__name__)
         assert caught, f"no pin catches mutant {name}"
+
+
+# ---- the native-FP8 MLA query quantisation --------------------------------
+import tests.test_oracle_q8_pins as qpins  # noqa: E402
+
+Q8_MUTANTS = {
+    "q8_scale_divisor": (
+        "const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;",
+        "const float sc = amax > 0.0f ? amax / 447.0f : 1.0f;"),
+    "q8_absmax_signed": (
+        "const float v = (float)fabs(pkv_oracle_bf16_to_f64(row[d]));",
+        "const float v = (float)pkv_oracle_bf16_to_f64(row[d]);"),
+    "q8_scale_ignored_by_verify": (
+        "const double sq = (double)a->q8_scale[r * a->qs_sr + h];",
+        "const double sq = 1.0;"),
+    "q8_head_stride_ignored": (
+        "const uint8_t *c8 = a->q8 + r * a->q8_sr + (int64_t)h * a->q8_sh;",
+        "const uint8_t *c8 = a->q8 + r * a->q8_sr;"),
+}
+
+Q8_BATTERY = [
+    (qpins.test_quantize_scale_is_absmax_over_448_in_fp32, {}),
+    (qpins.test_quantize_absmax_element_is_448, {}),
+    (qpins.test_quantize_zero_row_and_single_value, {}),
+    (qpins.test_quantize_matches_torch_float8_conversion_below_the_max, {}),
+    (qpins.test_quantize_error_within_half_a_step, {}),
+    (qpins.test_verify_q8_equals_verify_for_exactly_representable_queries, dict(shift=0)),
+    (qpins.test_verify_q8_equals_verify_for_exactly_representable_queries, dict(shift=3)),
+]
+
+
+@pytest.mark.parametrize("name", sorted(Q8_MUTANTS))
+def test_q8_mutant_is_caught(name, monkeypatch):
+    old, new = Q8_MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutant {name}: pattern must occur exactly once"
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, f"{name}.c")
+        with open(path, "w") as f:
+            f.write(src.replace(old, new))
+        lib = oracle.load(oracle.compile_oracle(path, os.path.join(tmp, f"lib{name}.so")))
+        monkeypatch.setattr(qpins, "LIB", lib)
+        caught = []
+        for fn, kw in Q8_BATTERY:
+            try:
+                fn(**kw)
+            except (AssertionError, oracle.OracleError):
+                caught.append(fn.__name__)
+        assert caught, f"no pin catches mutant {name}"
