@@ -319,6 +319,25 @@ def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
                      "tensor_frac_of_measured_bf16": fl / (med * 1e-3) / 1e12 / peak_tf,
                      "GBps": nbytes / (med * 1e-3) / 1e9, "flops": fl, "kv_bytes": nbytes,
                      "cap": prob.num_kv_splits}
+        if key == "mla_fp8" and want("native"):
+            # the same workload on the native-FP8 path: query quantised to e4m3
+            # per (row, head) inside the timed call, S on kind::f8f6f4 MMAs
+            q8 = torch.empty(tq.shape, dtype=torch.float8_e4m3fn, device=dev)
+            qs = torch.empty(tq.shape[:2], dtype=torch.float32, device=dev)
+
+            def fn_native():
+                pkv.mla_quantize_q(tq, q8, qs)
+                pkv.mla_verify_attn_fp8_native(q8, qs, tc, tbt, tsl, trl, prob.qlen, prob.scale,
+                                               prob.page_size, ks, out, lse, prob.num_kv_splits)
+            med_n, _ = time_events(fn_native, flush, steps)
+            res["mla_fp8_native_b128"] = {
+                "us": 1e3 * med_n, "TFLOPs": fl / (med_n * 1e-3) / 1e12,
+                "tensor_frac_of_measured_bf16": fl / (med_n * 1e-3) / 1e12 / peak_tf,
+                "GBps": nbytes / (med_n * 1e-3) / 1e9, "flops": fl, "kv_bytes": nbytes,
+                "cap": prob.num_kv_splits,
+                "note": "query quantised to e4m3 (an opt-in numerics change); the quantisation "
+                        "kernel is inside the timed call"}
+            del q8, qs
         del tq, tc
     if want("append"):
         # the cache write before each call: the Flint batch's current tokens
@@ -663,7 +682,8 @@ def main():
                     help="skip the other workloads (tiny, long context, MLA)")
     ap.add_argument("--extra-steps", type=int, default=30)
     ap.add_argument("--only", default="",
-                    help="comma list of tiny,long1,long8,mla,mla_fp8,append: time only these (no headline)")
+                    help="comma list of tiny,long1,long8,mla,mla_fp8,native (with mla_fp8),append: time only "
+                         "these (no headline)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

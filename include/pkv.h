@@ -2,7 +2,7 @@
  * pkv.h -- C ABI of libpkv: split-KV paged decode attention on GB300 (sm_103a).
  *
  * Two attention operations and the cache write that precedes them, each one
- * kernel launch on the caller's stream:
+ * or two kernel launches on the caller's stream:
  *
  *  - pkv_paged_decode_attn: GQA decode.  Every request has one query token per
  *    query head; it attends to the keys of its KV cache, gathered page by page
@@ -19,6 +19,10 @@
  *    FP8 e4m3 with a scalar dequantisation factor.  Defined by
  *    "vllm.v1.attention.ops.triton_decode_attention"
  *    (decode_attention_fwd_verify: parameters).
+ *
+ *  - pkv_mla_quantize_q + pkv_mla_verify_attn_fp8_native: the same MLA verify
+ *    over an FP8 cache with the query quantised to e4m3 per (row, head), so
+ *    that the score MMAs run on 8-bit operands (an opt-in numerics change).
  *
  *  - pkv_gqa_kv_append / pkv_mla_kv_append: the step before either call,
  *    writing the current token (or the verify tokens' latent rows) into the
@@ -216,6 +220,52 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
                                 const pkv_tensor* real_seq_lens, int qlen, float scale,
                                 int page_size, const pkv_tensor* k_scale, const pkv_tensor* out,
                                 const pkv_tensor* lse, int num_kv_splits, void* stream);
+
+/*
+ * pkv_mla_quantize_q -- per-(row, head) e4m3 quantisation of an MLA query, the
+ * input of pkv_mla_verify_attn_fp8_native.  The pages give no recipe (the
+ * verify page's FP8 path dequantises the cache by a scalar k_scale); this is
+ * the library's reading: with a = max |q[r, h, :]| over the 576 bf16 values,
+ * q_scale[r, h] = a / 448 in fp32 (round to nearest even; 1 when a = 0) and
+ * q8[r, h, d] = e4m3(q[r, h, d] / q_scale[r, h]), the quotient rounded to fp32
+ * (nearest even) and then to the nearest e4m3 value, ties to even, saturating
+ * at +-448; NaN stays NaN.  One launch.
+ *   q        bf16 [R, 128, 576], last dim contiguous, 16-byte aligned rows.
+ *   q8       FP8 e4m3 [R, 128, 576] (caller-owned output): heads contiguous
+ *            rows of 576 bytes, row stride a multiple of 16, 16-byte aligned.
+ *   q_scale  fp32 [R, 128] (caller-owned output), last dim contiguous.
+ *   stream   cudaStream_t.
+ * Errors: PKV_ERR_INVALID_ARG (shapes, dtypes), PKV_ERR_ALIGNMENT,
+ * PKV_ERR_UNSUPPORTED unless H == 128 and the last dim is 576; R == 0 is a
+ * no-op.
+ */
+PKV_API int pkv_mla_quantize_q(const pkv_tensor* q, const pkv_tensor* q8,
+                               const pkv_tensor* q_scale, void* stream);
+
+/*
+ * pkv_mla_verify_attn_fp8_native -- pkv_mla_verify_attn over an FP8 e4m3 cache
+ * with the query given as e4m3 codes q8 and per-(row, head) scales q_scale
+ * (pkv_mla_quantize_q): the query of (row r, head h) is code value x
+ * q_scale[r, h], and S = Q K^T runs as kind::f8f6f4 tensor-core MMAs on the
+ * raw e4m3 operands (scores scaled by q_scale x k_scale x scale afterwards).
+ * Everything else (row limits, softmax, P.V in bf16, split merge, out, lse) is
+ * pkv_mla_verify_attn's.  Source: "vllm.v1.attention.ops.
+ * triton_decode_attention", decode_attention_fwd_verify (parameters); the
+ * query quantisation is the library's, see pkv_mla_quantize_q.
+ *   q8, q_scale   as written by pkv_mla_quantize_q ([B*qlen, 128, 576] e4m3
+ *                 with 16-byte aligned rows; [B*qlen, 128] fp32).
+ *   latent_cache  FP8 e4m3 only (PKV_ERR_UNSUPPORTED for bf16).
+ *   other arguments as pkv_mla_verify_attn.
+ * Two launches (the unit plan, then the kernel).
+ */
+PKV_API int pkv_mla_verify_attn_fp8_native(const pkv_tensor* q8, const pkv_tensor* q_scale,
+                                           const pkv_tensor* latent_cache,
+                                           const pkv_tensor* block_table,
+                                           const pkv_tensor* seq_lens,
+                                           const pkv_tensor* real_seq_lens, int qlen, float scale,
+                                           int page_size, const pkv_tensor* k_scale,
+                                           const pkv_tensor* out, const pkv_tensor* lse,
+                                           int num_kv_splits, void* stream);
 
 /*
  * pkv_num_kv_splits -- static upper bound on KV splits, safe to bake into a

@@ -87,6 +87,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.pkv_paged_decode_attn.argtypes = [T, T, T, T, T, i32, f32, i32, i32, T, T, vp]
         lib.pkv_paged_decode_attn_noalloc.argtypes = [T, T, T, T, T, i32, f32, i32, i32, T, T, vp]
         lib.pkv_mla_verify_attn.argtypes = [T, T, T, T, T, i32, f32, i32, T, T, T, i32, vp]
+        lib.pkv_mla_quantize_q.argtypes = [T, T, T, vp]
+        lib.pkv_mla_verify_attn_fp8_native.argtypes = [T, T, T, T, T, T, i32, ctypes.c_float, i32, T,
+                                                       T, T, i32, vp]
         lib.pkv_gqa_kv_append.argtypes = [T, T, T, T, T, i32, vp]
         lib.pkv_mla_kv_append.argtypes = [T, T, T, T, i32, i32, T, vp]
         lib.pkv_num_kv_splits.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_double, i32, i32]
@@ -94,7 +97,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.pkv_check_counters.argtypes = [i32, ctypes.POINTER(ctypes.c_int64)]
         lib.pkv_last_error.restype = ctypes.c_char_p
         for name in ("pkv_init", "pkv_paged_decode_attn", "pkv_paged_decode_attn_noalloc",
-                     "pkv_mla_verify_attn", "pkv_gqa_kv_append", "pkv_mla_kv_append",
+                     "pkv_mla_verify_attn", "pkv_mla_quantize_q",
+                     "pkv_mla_verify_attn_fp8_native", "pkv_gqa_kv_append", "pkv_mla_kv_append",
                      "pkv_num_kv_splits", "pkv_check_errors", "pkv_check_counters",
                      "pkv_shutdown", "pkv_version"):
             getattr(lib, name).restype = i32
@@ -195,6 +199,27 @@ def mla_verify_attn(q, latent_cache, block_table, seq_lens, real_seq_lens, qlen,
         _desc(q), _desc(latent_cache), _desc(block_table), _desc(seq_lens),
         _desc(real_seq_lens), int(qlen), float(scale), int(page_size), _desc(k_scale),
         _desc(out), _desc(lse), int(num_kv_splits), _stream(stream, q)))
+    return out
+
+
+def mla_quantize_q(q, q8, q_scale, stream=None):
+    """Per-(row, head) e4m3 quantisation of an MLA query (C: pkv_mla_quantize_q):
+    writes ``q8`` (float8_e4m3fn [R, 128, 576]) and ``q_scale`` (fp32 [R, 128])."""
+    lib = load_library()
+    _check(lib.pkv_mla_quantize_q(_desc(q), _desc(q8), _desc(q_scale), _stream(stream, q)))
+    return q8, q_scale
+
+
+def mla_verify_attn_fp8_native(q8, q_scale, latent_cache, block_table, seq_lens, real_seq_lens,
+                               qlen, scale, page_size, k_scale, out, lse, num_kv_splits=0,
+                               stream=None):
+    """MLA causal verify over an e4m3 cache with an e4m3 query (C:
+    pkv_mla_verify_attn_fp8_native).  Writes ``out`` and ``lse`` in place."""
+    lib = load_library()
+    _check(lib.pkv_mla_verify_attn_fp8_native(
+        _desc(q8), _desc(q_scale), _desc(latent_cache), _desc(block_table), _desc(seq_lens),
+        _desc(real_seq_lens), int(qlen), float(scale), int(page_size), _desc(k_scale),
+        _desc(out), _desc(lse), int(num_kv_splits), _stream(stream, q8)))
     return out
 
 

@@ -473,15 +473,30 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
   return PKV_OK;
 }
 
-PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_cache,
-                                const pkv_tensor* block_table, const pkv_tensor* seq_lens,
-                                const pkv_tensor* real_seq_lens, int qlen, float scale,
-                                int page_size, const pkv_tensor* k_scale, const pkv_tensor* out,
-                                const pkv_tensor* lse, int num_kv_splits, void* stream_ptr) {
+// Both MLA verify entry points: q (bf16) for pkv_mla_verify_attn, or q8 (e4m3
+// codes) + q_scale for pkv_mla_verify_attn_fp8_native (native == true).
+static int mla_verify_impl(const pkv_tensor* q, const pkv_tensor* q8, const pkv_tensor* q_scale,
+                           bool native, const pkv_tensor* latent_cache,
+                           const pkv_tensor* block_table, const pkv_tensor* seq_lens,
+                           const pkv_tensor* real_seq_lens, int qlen, float scale, int page_size,
+                           const pkv_tensor* k_scale, const pkv_tensor* out, const pkv_tensor* lse,
+                           int num_kv_splits, void* stream_ptr) {
   int rc;
-  if ((rc = check_tensor(q, "q", PKV_DTYPE_BF16, 3))) return rc;
+  if (native) {
+    if ((rc = check_tensor(q8, "q8", PKV_DTYPE_FP8_E4M3, 3))) return rc;
+    if ((rc = check_tensor(q_scale, "q_scale", PKV_DTYPE_F32, 2))) return rc;
+    if (q8->stride[2] != 1 || q8->stride[0] % 16 || q8->stride[1] % 16 || !aligned16(q8->data))
+      return fail(PKV_ERR_ALIGNMENT, "q8 rows must be contiguous and 16-byte aligned");
+    if (q_scale->shape[0] != q8->shape[0] || q_scale->shape[1] != q8->shape[1])
+      return fail(PKV_ERR_INVALID_ARG, "q_scale must be [B*qlen, 128]");
+    q = q8;
+  } else if ((rc = check_tensor(q, "q", PKV_DTYPE_BF16, 3))) {
+    return rc;
+  }
   if (!latent_cache) return fail(PKV_ERR_INVALID_ARG, "latent_cache is NULL");
   const bool fp8 = latent_cache->dtype == PKV_DTYPE_FP8_E4M3;
+  if (native && !fp8)
+    return fail(PKV_ERR_UNSUPPORTED, "the native-FP8 path needs an e4m3 latent cache");
   if ((rc = check_tensor(latent_cache, "latent_cache", fp8 ? PKV_DTYPE_FP8_E4M3 : PKV_DTYPE_BF16,
                          latent_cache->ndim == 3 ? 3 : 4)))
     return rc;
@@ -544,8 +559,8 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
     return fail(PKV_ERR_INVALID_ARG, "lse must be [B*qlen, 128]");
   if (q->stride[2] != 1 || out->stride[2] != 1)
     return fail(PKV_ERR_INVALID_ARG, "q and out last dims must be contiguous");
-  if (q->stride[0] % 8 || q->stride[1] % 8 || out->stride[0] % 8 || out->stride[1] % 8 ||
-      !aligned16(q->data) || !aligned16(out->data))
+  if ((!native && (q->stride[0] % 8 || q->stride[1] % 8 || !aligned16(q->data))) ||
+      out->stride[0] % 8 || out->stride[1] % 8 || !aligned16(out->data))
     return fail(PKV_ERR_ALIGNMENT, "q and out must be 16-byte aligned with strides %% 8 == 0");
   if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
   if (num_kv_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_splits < 0");
@@ -582,38 +597,61 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
   EncodeTiledFn encode = nullptr;
   if ((rc = get_encoder(&encode))) return rc;
   CUtensorMap q_map, kv_map;
-  {
-    const cuuint64_t gdim[3] = {cuuint64_t(Lk), cuuint64_t(H), cuuint64_t(R)};
-    const cuuint64_t gstr[2] = {cuuint64_t(q->stride[1]) * 2, cuuint64_t(q->stride[0]) * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    CUresult cr = encode(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q->data, gdim, gstr, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) return fail(PKV_ERR_INVALID_ARG, "q tensor map rejected (%d)", (int)cr);
-  }
-  {
-    // the cache viewed as (64 dims, tokens, 9 chunks of 64 dims, pages): a box
-    // of (64, n tokens, 9, 1) lands chunk-major, n rows of 128 (bf16, 128-byte
-    // swizzle) or 64 (e4m3, plain) bytes per chunk
+  if (native) {
+    // the e4m3 cache as (64 dims, tokens, 9 chunks of 64 dims, pages): a box of
+    // (64, 8, 9, 1) lands chunk-major, 8 rows of 64 bytes per chunk, 64-byte swizzle
     const cuuint64_t gdim[4] = {64, cuuint64_t(page_size), 9, cuuint64_t(num_pages)};
-    const cuuint64_t gstr[3] = {cuuint64_t(s_tok) * esz, cuuint64_t(64 * esz),
-                                cuuint64_t(s_page) * esz};
-    const cuuint32_t box[4] = {64, fp8 ? 16u : 8u, 9, 1};
+    const cuuint64_t gstr[3] = {cuuint64_t(s_tok), 64, cuuint64_t(s_page)};
+    const cuuint32_t box[4] = {64, 8, 9, 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult cr = encode(&kv_map,
-                         fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                         latent_cache->data, gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult cr = encode(&kv_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, latent_cache->data, gdim, gstr,
+                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS)
       return fail(PKV_ERR_INVALID_ARG, "latent cache tensor map rejected (%d)", (int)cr);
+  } else {
+    {
+      const cuuint64_t gdim[3] = {cuuint64_t(Lk), cuuint64_t(H), cuuint64_t(R)};
+      const cuuint64_t gstr[2] = {cuuint64_t(q->stride[1]) * 2, cuuint64_t(q->stride[0]) * 2};
+      const cuuint32_t box[3] = {64, 128, 1};
+      const cuuint32_t es[3] = {1, 1, 1};
+      CUresult cr = encode(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q->data, gdim, gstr, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (cr != CUDA_SUCCESS) return fail(PKV_ERR_INVALID_ARG, "q tensor map rejected (%d)", (int)cr);
+    }
+    {
+      // the cache viewed as (64 dims, tokens, 9 chunks of 64 dims, pages): a box
+      // of (64, n tokens, 9, 1) lands chunk-major, n rows of 128 (bf16, 128-byte
+      // swizzle) or 64 (e4m3, plain) bytes per chunk
+      const cuuint64_t gdim[4] = {64, cuuint64_t(page_size), 9, cuuint64_t(num_pages)};
+      const cuuint64_t gstr[3] = {cuuint64_t(s_tok) * esz, cuuint64_t(64 * esz),
+                                  cuuint64_t(s_page) * esz};
+      const cuuint32_t box[4] = {64, fp8 ? 16u : 8u, 9, 1};
+      const cuuint32_t es[4] = {1, 1, 1, 1};
+      CUresult cr = encode(&kv_map,
+                           fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                           latent_cache->data, gdim, gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (cr != CUDA_SUCCESS)
+        return fail(PKV_ERR_INVALID_ARG, "latent cache tensor map rejected (%d)", (int)cr);
+    }
   }
   pkv::MlaParams p;
   std::memset(&p, 0, sizeof p);
-  p.q = static_cast<const uint16_t*>(q->data);
-  p.q_sr = q->stride[0];
-  p.q_sh = q->stride[1];
+  if (native) {
+    p.q8 = static_cast<const uint8_t*>(q8->data);
+    p.q8_sr = q8->stride[0];
+    p.q8_sh = q8->stride[1];
+    p.q_scale = static_cast<const float*>(q_scale->data);
+    p.qs_sr = q_scale->stride[0];
+    p.qs_sh = q_scale->stride[1];
+  } else {
+    p.q = static_cast<const uint16_t*>(q->data);
+    p.q_sr = q->stride[0];
+    p.q_sh = q->stride[1];
+  }
   p.kv = static_cast<const uint8_t*>(latent_cache->data);
   p.kv_stok = s_tok * esz;
   p.kv_spage = s_page * esz;
@@ -643,8 +681,74 @@ PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_ca
   p.err = ws.err;
   if ((rc = order_streams(st, stream, capturing))) return rc;
   const cudaError_t e =
-      pkv::launch_mla_verify(p, q_map, kv_map, fp8, int(units * cap), stream);
+      native ? pkv::launch_mla_verify_native(p, kv_map, int(units * cap), stream)
+             : pkv::launch_mla_verify(p, q_map, kv_map, fp8, int(units * cap), stream);
   if (e != cudaSuccess) return cuda_fail(e, "mla verify launch");
+  return PKV_OK;
+}
+
+PKV_API int pkv_mla_verify_attn(const pkv_tensor* q, const pkv_tensor* latent_cache,
+                                const pkv_tensor* block_table, const pkv_tensor* seq_lens,
+                                const pkv_tensor* real_seq_lens, int qlen, float scale,
+                                int page_size, const pkv_tensor* k_scale, const pkv_tensor* out,
+                                const pkv_tensor* lse, int num_kv_splits, void* stream_ptr) {
+  return mla_verify_impl(q, nullptr, nullptr, false, latent_cache, block_table, seq_lens,
+                         real_seq_lens, qlen, scale, page_size, k_scale, out, lse, num_kv_splits,
+                         stream_ptr);
+}
+
+PKV_API int pkv_mla_verify_attn_fp8_native(const pkv_tensor* q8, const pkv_tensor* q_scale,
+                                           const pkv_tensor* latent_cache,
+                                           const pkv_tensor* block_table,
+                                           const pkv_tensor* seq_lens,
+                                           const pkv_tensor* real_seq_lens, int qlen, float scale,
+                                           int page_size, const pkv_tensor* k_scale,
+                                           const pkv_tensor* out, const pkv_tensor* lse,
+                                           int num_kv_splits, void* stream_ptr) {
+  return mla_verify_impl(nullptr, q8, q_scale, true, latent_cache, block_table, seq_lens,
+                         real_seq_lens, qlen, scale, page_size, k_scale, out, lse, num_kv_splits,
+                         stream_ptr);
+}
+
+PKV_API int pkv_mla_quantize_q(const pkv_tensor* q, const pkv_tensor* q8,
+                               const pkv_tensor* q_scale, void* stream_ptr) {
+  int rc;
+  if ((rc = check_tensor(q, "q", PKV_DTYPE_BF16, 3))) return rc;
+  if ((rc = check_tensor(q8, "q8", PKV_DTYPE_FP8_E4M3, 3))) return rc;
+  if ((rc = check_tensor(q_scale, "q_scale", PKV_DTYPE_F32, 2))) return rc;
+  const int64_t R = q->shape[0], H = q->shape[1], Lk = q->shape[2];
+  if (H != pkv::kMlaHeads) return fail(PKV_ERR_UNSUPPORTED, "%lld heads (128 are built)", (long long)H);
+  if (Lk != pkv::kMlaLk) return fail(PKV_ERR_UNSUPPORTED, "Lk %lld (576 is built)", (long long)Lk);
+  if (q8->shape[0] != R || q8->shape[1] != H || q8->shape[2] != Lk || q_scale->shape[0] != R ||
+      q_scale->shape[1] != H)
+    return fail(PKV_ERR_INVALID_ARG, "q8 must be [R, 128, 576] and q_scale [R, 128]");
+  if (q->stride[2] != 1 || q->stride[0] % 8 || q->stride[1] % 8 || !aligned16(q->data))
+    return fail(PKV_ERR_ALIGNMENT, "q rows must be contiguous and 16-byte aligned");
+  if (q8->stride[2] != 1 || q8->stride[1] != Lk || q8->stride[0] % 16 || !aligned16(q8->data))
+    return fail(PKV_ERR_ALIGNMENT, "q8 heads must be contiguous rows of 576 bytes, 16-byte aligned");
+  if (q_scale->stride[1] != 1 && H > 1)
+    return fail(PKV_ERR_INVALID_ARG, "q_scale rows must be contiguous");
+  if (R == 0) return PKV_OK;
+  if (R * H >= (int64_t(1) << 31))
+    return fail(PKV_ERR_INVALID_ARG, "%lld (row, head) pairs", (long long)(R * H));
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int dev = 0;
+  DeviceState* st = nullptr;
+  bool capturing = false;
+  if ((rc = workspace_for(stream, &dev, &st, &capturing))) return rc;
+  pkv::QuantParams p;
+  p.q = static_cast<const uint16_t*>(q->data);
+  p.q_sr = q->stride[0];
+  p.q_sh = q->stride[1];
+  p.q8 = static_cast<uint8_t*>(q8->data);
+  p.q8_sr = q8->stride[0];
+  p.q_scale = static_cast<float*>(q_scale->data);
+  p.qs_sr = q_scale->stride[0];
+  p.R = int(R);
+  p.H = int(H);
+  if ((rc = order_streams(st, stream, capturing))) return rc;
+  const cudaError_t e = pkv::launch_mla_quantize_q(p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "mla quantize launch");
   return PKV_OK;
 }
 

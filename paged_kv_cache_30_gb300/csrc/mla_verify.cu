@@ -48,11 +48,13 @@
 #include "pkv_internal.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
+#include "mla_common.cuh"
 
 #include <cuda_fp16.h>
 
 namespace pkv {
 namespace {
+using namespace mla;
 
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kChunks = kMlaLk / 64;            // 9 64-dim chunks of a latent row
@@ -97,75 +99,6 @@ enum { kQFull = 0, kQtReady = 1, kKvFull = 2, kKvEmpty = 6, kSFull = 10, kSFree 
        kPvDone = 15, kF8Full = 16, kF8Empty = 20, kNumBars = 24 };
 constexpr int kMaxStages = 4;
 constexpr int kConverters = 192;  // FP8: six converter warps
-
-struct Unit {
-  int b, split, t, half, nsplit;
-  int L, lim;
-  int tile0, ntiles;  // tiles [tile0, tile0 + ntiles) of this CTA
-};
-
-__device__ __forceinline__ int clamped_len(const MlaParams& p, int b) {
-  int L = __ldg(p.seq_lens + b);
-  if (L < 0) L = 0;
-  if ((long long)L > (long long)p.max_blocks * p.page_size) L = p.max_blocks * p.page_size;
-  return L;
-}
-
-__device__ __forceinline__ int split_count(const MlaParams& p, int L) {
-  const int req_tiles = (L + kMlaTile - 1) / kMlaTile;
-  const int ns = (req_tiles + kMlaMinTiles - 1) / kMlaMinTiles;
-  return ns < 1 ? 1 : (ns > p.cap ? p.cap : ns);
-}
-
-// Tiles of the largest split of a request of L keys.
-__device__ __forceinline__ int split_tiles(const MlaParams& p, int L) {
-  const int req_tiles = (L + kMlaTile - 1) / kMlaTile;
-  const int ns = split_count(p, L);
-  return (req_tiles + ns - 1) / ns;
-}
-
-// The unit of this CTA, from the plan the planning kernel wrote: entry
-// ((b * qlen + t) * 2 + half) * 16 + split, or -1 (returned as split 0 of
-// nsplit 0: no unit).
-__device__ __forceinline__ Unit decode_unit(const MlaParams& p) {
-  Unit u;
-  const int v = __ldg(p.plan + blockIdx.x);
-  if (v < 0) {
-    u.split = 0;
-    u.nsplit = 0;
-    return u;
-  }
-  u.split = v & 15;
-  const int ch = v >> 4;
-  u.half = ch & 1;
-  const int rt = ch >> 1;
-  u.b = rt / p.qlen;
-  u.t = rt - u.b * p.qlen;
-  const int L = clamped_len(p, u.b);
-  int Lr = p.real_seq_lens ? __ldg(p.real_seq_lens + u.b) : L;
-  int lim = L - p.qlen + 1 + u.t;
-  if (Lr < lim) lim = Lr;
-  if (lim < 0) lim = 0;
-  u.L = L;
-  u.lim = lim;
-  const int req_tiles = (L + kMlaTile - 1) / kMlaTile;
-  const int ns = split_count(p, L);
-  u.nsplit = ns;
-  const int a = (int)((long long)req_tiles * u.split / ns);
-  const int e = (int)((long long)req_tiles * (u.split + 1) / ns);
-  const int lim_tiles = (lim + kMlaTile - 1) / kMlaTile;
-  u.tile0 = a;
-  u.ntiles = max(0, min(e, lim_tiles) - a);
-  return u;
-}
-
-__device__ __forceinline__ int counter_index(const MlaParams& p, const Unit& u) {
-  return (u.b * p.qlen + u.t) * 2 + u.half;
-}
-
-__device__ __forceinline__ long long slot_of(const MlaParams& p, const Unit& u, int split) {
-  return ((long long)(u.b * p.cap + split) * p.qlen + u.t) * 2 + u.half;
-}
 
 template <bool kFp8>
 __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
@@ -774,20 +707,26 @@ cudaError_t launch_pdl(Kernel* fn, int grid, int threads, int smem, cudaStream_t
 template <bool kFp8>
 cudaError_t launch_t(const MlaParams& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
                      int grid, cudaStream_t stream) {
-  static std::atomic<uint64_t> attr_done{0}, plan_attr_done{0};
+  static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = set_smem_attr_once(mla_verify_kernel<kFp8>, Cfg<kFp8>::kSmemBytes, attr_done);
   if (e != cudaSuccess) return e;
-  e = set_smem_attr_once(mla_plan_kernel, kPlanSortMax * 8, plan_attr_done);
-  if (e != cudaSuccess) return e;
-  int p2 = 1;
-  while (p2 < p.B) p2 <<= 1;
-  e = launch_pdl(mla_plan_kernel, 1, kPlanThreads, p.B > kPlanSortMax ? 0 : p2 * 8, stream, p, grid);
+  e = launch_mla_plan(p, grid, stream);
   if (e != cudaSuccess) return e;
   return launch_pdl(mla_verify_kernel<kFp8>, grid, Cfg<kFp8>::kThreads, Cfg<kFp8>::kSmemBytes,
                     stream, p, q_map, kv_map);
 }
 
 }  // namespace
+
+cudaError_t launch_mla_plan(const MlaParams& p, int grid, cudaStream_t stream) {
+  static std::atomic<uint64_t> plan_attr_done{0};
+  cudaError_t e = set_smem_attr_once(mla_plan_kernel, kPlanSortMax * 8, plan_attr_done);
+  if (e != cudaSuccess) return e;
+  int p2 = 1;
+  while (p2 < p.B) p2 <<= 1;
+  return launch_pdl(mla_plan_kernel, 1, kPlanThreads, p.B > kPlanSortMax ? 0 : p2 * 8, stream, p,
+                    grid);
+}
 
 cudaError_t launch_mla_verify(const MlaParams& p, const CUtensorMap& q_map,
                               const CUtensorMap& kv_map, bool fp8, int grid,

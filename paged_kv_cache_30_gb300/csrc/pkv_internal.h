@@ -125,10 +125,35 @@ struct MlaParams {
   int* counters;                 // [(b*qlen + t)*2 + half]
   int* plan;                     // [grid] unit of each CTA (written by the planning kernel)
   int* err;
+  // native FP8 (e4m3 query): codes [B*qlen, 128, 576] and fp32 scales [B*qlen, 128]
+  const uint8_t* q8;
+  int64_t q8_sr, q8_sh;
+  const float* q_scale;
+  int64_t qs_sr, qs_sh;
 };
 
+// The planning kernel: writes p.plan[0, grid) (one CTA; programmatic dependent launch).
+cudaError_t launch_mla_plan(const MlaParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_mla_verify(const MlaParams& p, const CUtensorMap& q_map,
                               const CUtensorMap& kv_map, bool fp8, int grid, cudaStream_t stream);
+// Native FP8: planning kernel, then the verify kernel with S = Q8 K8^T on
+// kind::f8f6f4 (kv_map: the e4m3 cache as (64 dims, token, 9 chunks, page) with
+// a box of (64, 8, 9, 1) and 64-byte swizzle).
+cudaError_t launch_mla_verify_native(const MlaParams& p, const CUtensorMap& kv_map, int grid,
+                                     cudaStream_t stream);
+
+// Per-(row, head) e4m3 quantisation of an MLA query: scale = absmax / 448,
+// code = e4m3(q / scale) (round to nearest even, saturating).
+struct QuantParams {
+  const uint16_t* q;      // bf16 [R, H, 576]
+  int64_t q_sr, q_sh;     // element strides
+  uint8_t* q8;            // [R, H, 576], row stride q8_sr, head stride 576
+  int64_t q8_sr;
+  float* q_scale;         // [R, H], row stride qs_sr, head stride 1
+  int64_t qs_sr;
+  int R, H;
+};
+cudaError_t launch_mla_quantize_q(const QuantParams& p, cudaStream_t stream);
 
 // ---------------------------------------------------------- KV append --
 struct AppendParams {

@@ -194,3 +194,55 @@ def test_mla_append_validation(lib):
     empty = _t([0, 576], pkv.DTYPE_BF16)
     bt0, sl0 = _t([0, 8], pkv.DTYPE_I32), _t([0], pkv.DTYPE_I32)
     assert lib.pkv_mla_kv_append(r(empty), r(cache), r(bt0), r(sl0), 2, 16, None, None) == 0
+
+
+# --------------------------------------------------- native-FP8 MLA path --
+def _nat_args(R=4, P=16):
+    return dict(
+        q8=_t([R, 128, 576], pkv.DTYPE_FP8), qs=_t([R, 128], pkv.DTYPE_F32, ptr=0x30000),
+        c=_t([64, P, 1, 576], pkv.DTYPE_FP8), bt=_t([R, 8], pkv.DTYPE_I32),
+        sl=_t([R], pkv.DTYPE_I32), out=_t([R, 128, 512], pkv.DTYPE_BF16, ptr=0x20000),
+        lse=_t([R, 128], pkv.DTYPE_F32, ptr=0x40000))
+
+
+def _nat_call(lib, a, qlen=1, P=16):
+    r = ctypes.byref
+    return lib.pkv_mla_verify_attn_fp8_native(r(a["q8"]), r(a["qs"]), r(a["c"]), r(a["bt"]),
+                                              r(a["sl"]), None, qlen, 0.07, P, None,
+                                              r(a["out"]), r(a["lse"]), 0, None)
+
+
+@pytest.mark.parametrize("mutate,code", [
+    (lambda a: a.update(c=_t([64, 16, 1, 576], pkv.DTYPE_BF16)), -2),          # bf16 cache
+    (lambda a: a.update(q8=_t([4, 128, 576], pkv.DTYPE_BF16)), -1),            # q8 dtype
+    (lambda a: a.update(q8=_t([4, 128, 576], pkv.DTYPE_FP8, ptr=0x10008)), -3),  # misaligned
+    (lambda a: a.update(q8=_t([4, 128, 576], pkv.DTYPE_FP8, [73736, 576, 1])), -3),  # row stride
+    (lambda a: a.update(qs=_t([4, 64], pkv.DTYPE_F32)), -1),                   # scale shape
+    (lambda a: a.update(q8=_t([4, 64, 576], pkv.DTYPE_FP8),
+                        qs=_t([4, 64], pkv.DTYPE_F32)), -2),                   # 64 heads
+])
+def test_native_validation_rejects_before_any_cuda_call(lib, mutate, code):
+    a = _nat_args()
+    mutate(a)
+    assert _nat_call(lib, a) == code
+    assert pkv.last_error()
+
+
+def test_native_empty_batch_is_a_no_op(lib):
+    assert _nat_call(lib, _nat_args(R=0)) == 0
+
+
+@pytest.mark.parametrize("mutate,code", [
+    (lambda a: a.update(q=_t([4, 128, 512], pkv.DTYPE_BF16)), -2),             # Lk 512
+    (lambda a: a.update(q8=_t([4, 128, 576], pkv.DTYPE_FP8, [73728, 577, 1])), -3),
+    (lambda a: a.update(q8=_t([4, 128, 576], pkv.DTYPE_FP8, ptr=0x10004)), -3),
+    (lambda a: a.update(qs=_t([4, 128], pkv.DTYPE_BF16)), -1),
+    (lambda a: a.update(q=_t([4, 128, 576], pkv.DTYPE_BF16, ptr=0x10002)), -3),
+])
+def test_quantize_validation_rejects_before_any_cuda_call(lib, mutate, code):
+    a = dict(q=_t([4, 128, 576], pkv.DTYPE_BF16), q8=_t([4, 128, 576], pkv.DTYPE_FP8, ptr=0x50000),
+             qs=_t([4, 128], pkv.DTYPE_F32, ptr=0x60000))
+    mutate(a)
+    r = ctypes.byref
+    assert lib.pkv_mla_quantize_q(r(a["q"]), r(a["q8"]), r(a["qs"]), None) == code
+    assert pkv.last_error()
