@@ -48,7 +48,7 @@ constexpr int kConverters = 192;
 constexpr int kOffF8 = 0;
 constexpr int kOffV = kOffF8 + kF8Stages * kF8Tile;  // 73728
 constexpr int kOffP = kOffV + kVStages * kVTile;     // 122880
-constexpr int kOffBars = kOffP + kPBytes;            // 131072
+constexpr int kOffBars = kOffP + 2 * kPBytes;        // 139264: P of tile i in buffer i % 2
 constexpr int kSmemBytes = kOffBars + 256 + 1024;
 static_assert(kOffV % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms need 1024 B alignment");
 
@@ -62,7 +62,7 @@ constexpr float kRescaleLog2 = 8.0f;
 // barrier indices: a tile's e4m3 stage is free once S has read it (MMA commit)
 // and the converters have expanded its V half (count 2)
 enum { kQReady = 0, kF8Full = 1, kF8Empty = 5, kVFull = 9, kVEmpty = 12, kSFull = 15,
-       kSFree = 17, kPFull = 19, kPvDone = 20, kNumBars = 21 };
+       kSFree = 17, kPFull = 19, kPFree = 21, kPvDone = 23, kNumBars = 24 };
 
 __global__ void __launch_bounds__(kThreads, 1)
     mla_verify_native_kernel(const __grid_constant__ MlaParams p,
@@ -96,8 +96,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kSFull + s), 1);
       mbar_init(bar(kSFree + s), 128);
+      mbar_init(bar(kPFull + s), 1);
+      mbar_init(bar(kPFree + s), 1);
     }
-    mbar_init(bar(kPFull), 1);
     mbar_init(bar(kPvDone), 1);
     fence_barrier_init();
   }
@@ -205,17 +206,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_q8_share();
       mbar_wait(bar(kQReady), 0, p.err);
       auto do_pv = [&](int j) {
-        const int sv = j % kVStages;
+        const int sv = j % kVStages, pb = j & 1;
         mbar_wait(bar(kVFull + sv), (j / kVStages) & 1, p.err);
-        mbar_wait(bar(kPFull), j & 1, p.err);
+        mbar_wait(bar(kPFull + pb), (j >> 1) & 1, p.err);
         tc::fence_after_sync();
         const uint32_t v0 = sV + sv * kVTile;
 #pragma unroll
         for (int ks = 0; ks < kMlaTile / 16; ++ks)
-          tc::mma_bf16_elect(tmem + kTmemO, tc::smem_desc(sP + ks * 32, 16, 512, tc::kSwizzle64),
+          tc::mma_bf16_elect(tmem + kTmemO,
+                             tc::smem_desc(sP + pb * kPBytes + ks * 32, 16, 512, tc::kSwizzle64),
                              tc::smem_desc(v0 + ks * 2 * kVGroup, 1024, kVGroup, tc::kSwizzle128),
                              id_pv, j > 0 || ks > 0);
         tc::commit_elect(bar(kPvDone));
+        tc::commit_elect(bar(kPFree + pb));
         tc::commit_elect(bar(kVEmpty + sv));
       };
       for (int i = 0; i < n; ++i) {
@@ -295,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float s_eff = __ldg(p.q_scale + qrow * p.qs_sr + (long long)row * p.qs_sh) * k_scale * p.scale;
     const float c2 = s_eff * kLog2e;
     float m_used = -INFINITY, l = 0.f;
-    uint8_t* p_row = base + kOffP + (row / 8) * 512 + (row % 8) * 64;
+    // P row of this head in buffer b (64-byte swizzle)
+    auto p_row = [&](int b) { return base + kOffP + b * kPBytes + (row / 8) * 512 + (row % 8) * 64; };
     const int pswz = (row % 8) >> 1;
     if (n > 0) load_q8_share();
     for (int i = 0; i < n; ++i) {
@@ -308,13 +312,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::wait_ld();
       tc::fence_before_sync();
       mbar_arrive(bar(kSFree + sb));
+      // P buffer i % 2 is free once P V of tile i - 2 is done.  Waiting here,
+      // before any kPvDone wait, also keeps kPvDone within one phase of the
+      // P V this thread waits for (parity waits cannot alias).
+      const int pb = i & 1;
+      mbar_wait(bar(kPFree + pb), ((i >> 1) & 1) ^ 1u, p.err);
       const int nvalid = min(kMlaTile, u.lim - (u.tile0 + i) * kMlaTile);
       float mt = -INFINITY;
 #pragma unroll
       for (int c = 0; c < kMlaTile; ++c)
         if (c < nvalid) mt = fmaxf(mt, __uint_as_float(xr[c]));
       // lazy max, as in mla_verify.cu (the warp rescales its O rows together)
-      bool waited = false;
       const bool need =
           mt > -INFINITY && (m_used == -INFINITY || (mt - m_used) * c2 > kRescaleLog2);
       if (__any_sync(0xffffffffu, need)) {
@@ -323,7 +331,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             (m_used == -INFINITY) ? 0.f : (need ? ex2((m_used - m_new) * c2) : 1.f);
         if (i > 0) {
           mbar_wait(bar(kPvDone), (i - 1) & 1, p.err);
-          waited = true;
           __syncwarp();
           tc::fence_after_sync();
           for (int j = 0; j < kMlaHalf / 32; ++j) {
@@ -352,20 +359,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[c / 2] = pack_bf16(e0, e1);
       }
       l += lt;
-      if (i > 0 && !waited) mbar_wait(bar(kPvDone), (i - 1) & 1, p.err);
 #pragma unroll
       for (int uq = 0; uq < 4; ++uq)
-        *reinterpret_cast<uint4*>(p_row + ((uq ^ pswz) & 3) * 16) =
+        *reinterpret_cast<uint4*>(p_row(pb) + ((uq ^ pswz) & 3) * 16) =
             make_uint4(pk[4 * uq], pk[4 * uq + 1], pk[4 * uq + 2], pk[4 * uq + 3]);
       fence_proxy_async_smem();  // P is read by the MMA (async proxy)
       tc::fence_before_sync();   // and any in-place O rescale precedes the next P V
       __syncwarp();
       named_bar_sync(1, 128);
-      if (row == 0) mbar_arrive(bar(kPFull));
+      if (row == 0) mbar_arrive(bar(kPFull + pb));
     }
 
     // ------------------------------ epilogue ------------------------------
     if (n > 0) {
+      // P V of tile n - 3 is done (the last kPFree wait): kPvDone is at most
+      // two phases short of the end
+      if (n >= 2) mbar_wait(bar(kPvDone), (n - 2) & 1, p.err);
       mbar_wait(bar(kPvDone), (n - 1) & 1, p.err);
       __syncwarp();
       tc::fence_after_sync();
