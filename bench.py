@@ -9,9 +9,10 @@ workload's two layer types -- a full-attention layer and a sliding-window
 
 Prints one JSON line (rank 0).  `value` is KV-cache GB/s over the step
 (algorithmic bytes: attended tokens x Hkv x 512 B) with inputs resident in HBM
-and L2 flushed between steps; `e2e` repeats the measurement through the same C
-ABI call with the step's inputs copied from pinned host memory and the
-outputs copied back inside the timed region.  `roofline` covers the dominant
+and no L2 flush (each step streams 797 MB of KV, over six times the 129 MB L2);
+`e2e` repeats the measurement through the same C ABI call with the step's
+inputs copied from pinned host memory and the outputs copied back inside the
+timed region.  `roofline` covers the dominant
 kernel (the full-attention layer) against the measured HBM copy bandwidth.
 `cpu_baseline` is the fp64 CPU oracle timed on this host on a bounded sample.
 
@@ -209,11 +210,33 @@ def mla_flops(prob) -> float:
     return float(tot) * 128 * 2 * (576 + 512)
 
 
+class L2Flush:
+    """Evicts L2 between timed calls, outside the timed events: a 512 MiB write
+    (the eviction), then a read of another 512 MiB buffer so that the lines L2
+    holds afterwards are clean.  After the write alone the next kernel pays the
+    write-back of the flush's ~129 MB of dirty lines: the Flint full layer took
+    146.9 us after a write-only flush, 133.5 us after this one and 134.1 us
+    with no flush at all (its 777 MB exceed L2), and a per-CTA trace showed it
+    reading at 5.3 TB/s for its first 40 us after the write-only flush against
+    7.0 TB/s after this one."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self, s: int = 0):
+        import torch
+        self.w.fill_(float(s & 7))
+        torch.amax(self.r, dim=0, out=self.sink)
+
+
 def time_events(fn, flush, steps, warmup=3):
     import torch
     for _ in range(warmup):
         fn()
-        flush.fill_(1.0)
+        flush(1)
     ev = []
     for s in range(steps):
         a = torch.cuda.Event(enable_timing=True)
@@ -221,7 +244,7 @@ def time_events(fn, flush, steps, warmup=3):
         a.record()
         fn()
         b.record()
-        flush.fill_(float(s & 7))
+        flush(s)
         ev.append((a, b))
     torch.cuda.synchronize()
     ms = sorted(x.elapsed_time(y) for x, y in ev)
@@ -260,7 +283,7 @@ def _tiny(dev, flush, steps, tiny, gqa_entry):
 
 def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
     """Every other workload of the pages' problem, timed the same way (inputs
-    resident, L2 flushed between calls, CUDA events): the tiny decode batch,
+    resident, L2 flushed between calls by L2Flush, CUDA events): the tiny decode batch,
     the 131072-token long context at B=1 and B=8 across split caps, the two
     MLA verify workloads (bf16 and FP8 latent caches) and the paged KV append
     that precedes a decode or verify call."""
@@ -463,7 +486,7 @@ def run_gpu(args, rank, world, local_rank):
 
     if args.only:
         # profiling aid: time only the named other workloads
-        flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        flush = L2Flush(dev)
         peak, _ = measured_peaks()
         res = other_workloads(dev, flush, peak, measured_bf16_tflops(), args.extra_steps,
                               only=set(args.only.split(",")))
@@ -483,7 +506,7 @@ def run_gpu(args, rank, world, local_rank):
         d.append(dict(q=p.q.to(dev), kv=p.kv_cache.to(dev), bt=bt_dev, sl=sl_dev,
                       sinks=p.sinks.to(dev), out=torch.empty_like(p.q, device=dev),
                       lse=torch.empty(p.q.shape[:2], device=dev)))
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)  # for the other workloads; the step loop needs none
 
     def call(i):
         p, t = layers[i], d[i]
@@ -499,7 +522,6 @@ def run_gpu(args, rank, world, local_rank):
     # ---------------- device-resident timing ----------------
     for _ in range(args.warmup):
         call(0); call(1)
-        flush.fill_(1.0)
     assert pkv.check_errors(local_rank) == 0
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
@@ -514,7 +536,8 @@ def run_gpu(args, rank, world, local_rank):
         e[1].record(stream)
         call(1)
         e[2].record(stream)
-        flush.fill_(float(s & 7))  # outside the events: evicts L2 between steps
+        # no flush: the full layer's 777 MB of KV evict the window layer's 20 MB
+        # between its calls, and each step streams over six times the L2
     barrier()
     t1 = time.time()
     time.sleep(0.2)
@@ -645,9 +668,10 @@ def run_gpu(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "global_batch": 64 * world, "seed": args.seed,
                    "kv_bytes_per_step": step_bytes, "kv_bytes_full_layer": kv_bytes[0],
-                   "l2": "flushed between steps (512 MiB write outside the timed events); "
-                         "e2e loop: inputs larger than L2 (777 MB of KV per step), copies "
-                         "double-buffered on a second stream",
+                   "l2": "inputs larger than L2: no flush between steps (797 MB of KV per "
+                         "step, L2 129 MB); e2e loop the same, copies double-buffered on a "
+                         "second stream; other_workloads: L2 flushed between calls (512 MiB "
+                         "write, then a 512 MiB read so L2 is left clean)",
                    "parallelism": f"{world} independent ranks" if world > 1 else "single GPU"},
         "calls_per_s": calls_per_s,
         "hbm_frac_of_measured": value / peak,

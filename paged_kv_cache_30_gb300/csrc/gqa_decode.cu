@@ -8,7 +8,7 @@
 // module's numerics paragraph; block-table indexing as in the transformers
 // "Atencion paginada" decode path).
 //
-// Design: persistent, two CTAs per SM, each 1 producer warp + 4 consumer warps.
+// Design: persistent, two CTAs per SM, each 2 producer warps + 4 consumer warps.
 //  * Work items are (request, kv head, split) triples.  Every CTA derives the
 //    same item list in its prologue from seq_lens alone: request b's n_b
 //    attended pages are cut into s_b = min(cap, ceil(n_b / chunk)) contiguous
@@ -16,13 +16,16 @@
 //    target_items items (shorter requests use fewer splits).  CTAs pull items
 //    from a global queue (atomic head, reset by the last CTA to exit), so the
 //    launch shape depends only on the device and the batch.
-//  * The producer warp bulk-copies the item's 8 query rows into a descriptor
-//    slot, reads block-table entries 32 at a time and streams every 16-token
-//    tile of every page with one TMA operation -- a 5-D view of the cache
-//    (64 dims, token, 4 chunks of 64 dims, kv head, block) whose box lands the
-//    tile chunk-major as four 16 x 128-byte slabs (K lo, K hi, V lo, V hi) with
-//    128-byte swizzle -- into an 8-stage ring (8 KB stages) guarded by
-//    full/empty mbarriers.  It runs ahead across item boundaries.
+//  * The first producer warp takes items from the queue, writes each item's
+//    descriptor and bulk-copies its 8 query rows into a descriptor slot.  Both
+//    producer warps read block-table entries 32 at a time and stream the
+//    16-token tiles of every page with one TMA operation each -- the first the
+//    even pages, the second the odd ones (one issuing thread tops out near
+//    31 GB/s of 8 KB tiles, two reach ~49 GB/s) -- through a 5-D view of the
+//    cache (64 dims, token, 4 chunks of 64 dims, kv head, block) whose box
+//    lands the tile chunk-major as four 16 x 128-byte slabs (K lo, K hi, V lo,
+//    V hi) with 128-byte swizzle, into an 8-stage ring (8 KB stages) guarded
+//    by full/empty mbarriers.  They run ahead across item boundaries.
 //  * Consumer warp w takes tiles w, w+4, ... of the item.  It pulls the tile's
 //    K and V fragments into registers with ldmatrix (conflict-free thanks to
 //    the swizzle), frees the stage at once (after a generic-to-async proxy
@@ -47,7 +50,8 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kProducerWarps = 2;     // even and odd tiles
+constexpr int kThreads = kConsumers + 32 * kProducerWarps;
 constexpr int kCtasPerSm = 2;
 constexpr int kStageBytes = 16 * 512;  // one 16-token tile: 16 x [K | V] x bf16
 constexpr int kStages = 8;
@@ -69,7 +73,7 @@ constexpr int kOffQ = kOffWbuf + kConsumerWarps * kWbFloats * 4;
 constexpr int kOffPrefix = kOffQ + kItemSlots * kQBytes;
 constexpr int kOffItems = kOffPrefix + ((kGqaMaxBatch + 1) * 4 + 15) / 16 * 16;
 constexpr int kOffBars = kOffItems + kItemSlots * (int)sizeof(ItemDesc);
-constexpr int kNumBars = 2 * kStages + 2 * kItemSlots;
+constexpr int kNumBars = 2 * kStages + 3 * kItemSlots;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 static_assert(kOffWbuf % 1024 == 0 && kOffQ % 16 == 0 && kOffPrefix % 16 == 0 &&
@@ -77,6 +81,7 @@ static_assert(kOffWbuf % 1024 == 0 && kOffQ % 16 == 0 && kOffPrefix % 16 == 0 &&
               "shared-memory offsets");
 static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 static_assert(kMergeGroup * kGqaMlFloats <= kConsumerWarps * kWbFloats, "merge scratch");
+static_assert(kStages % (2 * kProducerWarps) == 0, "each stage is refilled by one producer warp");
 
 // Exclusive scan of one int per thread over the CTA; `scratch` holds one int
 // per warp plus one.  Returns the exclusive prefix; *total = the sum.
@@ -202,6 +207,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
   auto ifull_bar = [&](int s) { return bars + 8u * (2 * kStages + s); };
   auto iempty_bar = [&](int s) { return bars + 8u * (2 * kStages + kItemSlots + s); };
+  // descriptor written (no query bytes): what the second producer waits for
+  auto dfull_bar = [&](int s) { return bars + 8u * (2 * kStages + 2 * kItemSlots + s); };
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -212,7 +219,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     for (int s = 0; s < kItemSlots; ++s) {
       mbar_init(ifull_bar(s), 1);
-      mbar_init(iempty_bar(s), kConsumerWarps);
+      mbar_init(iempty_bar(s), kConsumerWarps + 1);  // + the second producer
+      mbar_init(dfull_bar(s), 1);
     }
     fence_barrier_init();
   }
@@ -260,8 +268,54 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   __syncthreads();
 
+  // Streams the tiles of pages [p0, p1) of (request row bt_row, kv head kvh)
+  // that fall to producer `mine`: whole pages, alternating (an item's first
+  // tile number `seq` is a multiple of TPP, so a page's tiles share a parity
+  // of seq / TPP and every ring stage is refilled by one producer only).
+  auto stream_tiles = [&](const int32_t* bt_row, int kvh, int p0, int p1, uint32_t seq,
+                          uint32_t mine) {
+    for (int pb = p0; pb < p1; pb += 32) {
+      const int cnt = min(32, p1 - pb);
+      int blk = 0;
+      if (lane < cnt) {
+        blk = __ldg(bt_row + pb + lane);
+        if (blk < 0 || blk >= p.num_blocks) atomicOr(p.err, DEVERR_BAD_BLOCK);
+      }
+      for (int i = 0; i < cnt; ++i) {
+        const int blk_i = __shfl_sync(0xffffffffu, blk, i);
+#pragma unroll
+        for (int sub = 0; sub < TPP; ++sub) {
+          if (lane == 0 && ((seq / TPP) & 1u) == mine) {
+            const int stage = seq % kStages;
+            mbar_wait(empty_bar(stage), ((seq / kStages) & 1) ^ 1u, p.err);
+            mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+            const uint32_t dst = ring + stage * kStageBytes;
+            // one box: 16 tokens x 4 chunks of 64 dims (K lo, K hi, V lo, V hi),
+            // landing chunk-major
+            tma_load_5d(dst, &kv_map, full_bar(stage), 0, 16 * sub, 0, kvh, blk_i);
+          }
+          ++seq;
+        }
+      }
+    }
+  };
+
+  if (warp == kConsumerWarps + 1) {
+    // ===================== second producer warp: odd tiles =====================
+    for (int it = 0;; ++it) {
+      const int slot = it % kItemSlots;
+      mbar_wait(dfull_bar(slot), (it / kItemSlots) & 1, p.err);
+      const ItemDesc d = items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(iempty_bar(slot));
+      if (d.item < 0) break;
+      stream_tiles(p.bt + (long long)d.b * p.bt_sb, d.kvh, d.p0, d.p1, (uint32_t)d.seq_base, 1u);
+    }
+    return;
+  }
+
   if (warp == kConsumerWarps) {
-    // =========================== producer warp ===========================
+    // ============ first producer warp: the queue, descriptors, even tiles ============
     int next = 0;
     if (lane == 0) next = atomicAdd(&p.sched[0], 1);
     next = __shfl_sync(0xffffffffu, next, 0);
@@ -279,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (lane == 0) {
           griddep_launch_dependents();  // the queue is empty: this CTA only drains now
           items[slot].item = -1;
+          mbar_arrive(dfull_bar(slot));
           mbar_arrive(ifull_bar(slot));
         }
         break;
@@ -302,8 +357,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         ItemDesc& d = items[slot];
         d.item = item; d.b = b; d.kvh = kvh; d.split = split; d.nsplit = nsplit;
         d.p0 = p0; d.p1 = p1; d.start_tok = start_tok; d.L = L; d.seq_base = (int)seq;
-        // the descriptor stores are released by this arrive; the phase also
-        // waits for the 8 query rows
+        // the descriptor stores are released by these arrives; the consumers'
+        // phase also waits for the 8 query rows
+        mbar_arrive(dfull_bar(slot));
         mbar_arrive_expect_tx(ifull_bar(slot), kQBytes);
         const uint16_t* qrow = p.q + b * p.q_sb + (long long)(kvh * kGqaGroup) * p.q_sh;
 #pragma unroll
@@ -311,35 +367,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           bulk_load(qbuf + slot * kQBytes + h * kGqaHeadDim * 2, qrow + h * p.q_sh,
                     kGqaHeadDim * 2, ifull_bar(slot));
       }
-      const int32_t* bt_row = p.bt + (long long)b * p.bt_sb;
-      for (int pb = p0; pb < p1; pb += 32) {
-        const int cnt = min(32, p1 - pb);
-        int blk = 0;
-        if (lane < cnt) {
-          blk = __ldg(bt_row + pb + lane);
-          if (blk < 0 || blk >= p.num_blocks) atomicOr(p.err, DEVERR_BAD_BLOCK);
-        }
-        for (int i = 0; i < cnt; ++i) {
-          const int blk_i = __shfl_sync(0xffffffffu, blk, i);
-#pragma unroll
-          for (int sub = 0; sub < TPP; ++sub) {
-            if (lane == 0) {
-              const int stage = seq % kStages;
-              mbar_wait(empty_bar(stage), ((seq / kStages) & 1) ^ 1u, p.err);
-              mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
-              const uint32_t dst = ring + stage * kStageBytes;
-              // one box: 16 tokens x 4 chunks of 64 dims (K lo, K hi, V lo, V hi),
-              // landing chunk-major
-              tma_load_5d(dst, &kv_map, full_bar(stage), 0, 16 * sub, 0, kvh, blk_i);
-            }
-            ++seq;
-          }
-        }
-      }
+      stream_tiles(p.bt + (long long)b * p.bt_sb, kvh, p0, p1, seq, 0u);
+      seq += (uint32_t)((p1 - p0) * TPP);
     }
     if (lane == 0) {
-      // every issued copy has landed before the CTA may exit (the consumers
-      // waited on them already unless a wait gave up)
+      // every issued copy (of both producer warps) has landed before the CTA
+      // may exit (the consumers waited on them already unless a wait gave up)
       const uint32_t recent = seq < (uint32_t)kStages ? seq : (uint32_t)kStages;
       for (uint32_t k = seq - recent; k < seq; ++k)
         mbar_wait(full_bar(k % kStages), (k / kStages) & 1, p.err);
