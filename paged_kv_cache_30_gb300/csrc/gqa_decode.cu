@@ -14,8 +14,10 @@
 //    attended pages are cut into s_b = min(cap, ceil(n_b / chunk)) contiguous
 //    page ranges, with chunk chosen from the total so that the launch has about
 //    target_items items (shorter requests use fewer splits).  CTAs pull items
-//    from a global queue (atomic head, reset by the last CTA to exit), so the
-//    launch shape depends only on the device and the batch.
+//    from a global queue (an atomic head; every CTA fetches until it draws an
+//    index past the end, so the launch makes exactly items + CTAs fetches and
+//    the CTA that draws the last one resets the head to zero), so the launch
+//    shape depends only on the device and the batch.
 //  * The first producer warp takes items from the queue, writes each item's
 //    descriptor and bulk-copies its 8 query rows into a descriptor slot.  Both
 //    producer warps read block-table entries 32 at a time and stream the
@@ -229,6 +231,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // and the kernel parameters; the inputs and the workspace are read after the
   // grids this launch depends on (e.g. the previous call) have completed.
   griddep_wait();
+  // The first queue fetch is issued now: its latency overlaps the prologue.
+  int first_item = 0;
+  if (warp == kConsumerWarps && lane == 0) first_item = atomicAdd(&p.sched[0], 1);
 
   // ---- prologue: the item list, identical in every CTA -------------------
   const int B = p.B;
@@ -316,14 +321,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   if (warp == kConsumerWarps) {
     // ============ first producer warp: the queue, descriptors, even tiles ============
-    int next = 0;
-    if (lane == 0) next = atomicAdd(&p.sched[0], 1);
-    next = __shfl_sync(0xffffffffu, next, 0);
+    // The fetch that returns total_items + gridDim.x - 1 is the launch's last
+    // (each CTA stops after its first index past the end): it resets the head.
+    const int last_fetch = total_items + (int)gridDim.x - 1;
+    if (lane == 0 && first_item == last_fetch) atomicExch(&p.sched[0], 0);
+    int next = __shfl_sync(0xffffffffu, first_item, 0);
     uint32_t seq = 0;
     for (int it = 0;; ++it) {
       const int item = next;
       if (item < total_items) {
-        if (lane == 0) next = atomicAdd(&p.sched[0], 1);
+        if (lane == 0) {
+          next = atomicAdd(&p.sched[0], 1);
+          if (next == last_fetch) atomicExch(&p.sched[0], 0);
+        }
         next = __shfl_sync(0xffffffffu, next, 0);
       }
       const int slot = it % kItemSlots;
@@ -376,12 +386,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const uint32_t recent = seq < (uint32_t)kStages ? seq : (uint32_t)kStages;
       for (uint32_t k = seq - recent; k < seq; ++k)
         mbar_wait(full_bar(k % kStages), (k / kStages) & 1, p.err);
-      // the last CTA out resets the queue for the next launch
-      __threadfence();
-      if (atomicAdd(&p.sched[1], 1) == (int)gridDim.x - 1) {
-        atomicExch(&p.sched[0], 0);
-        atomicExch(&p.sched[1], 0);
-      }
     }
     return;
   }

@@ -88,7 +88,7 @@ extern "C" PKV_API int pkv_paged_decode_attn_noalloc(
 
   pkv::GqaParams& p = call.p;
   int* words = reinterpret_cast<int*>(st.ptr);
-  p.sched = words;                      // [0] queue head, [1] exited CTAs
+  p.sched = words;                      // [0] queue head
   p.err = words + 32;                   // device error bits (not reported on this path)
   p.counters = words + 64;              // [kMaxPairs]
   p.group_counters = words + 64 + kMaxPairs;  // [kMaxItems]

@@ -28,7 +28,7 @@ struct Workspace {
   size_t partial_bytes = 0;
   int* counters = nullptr;    // self-resetting arrival counters
   int64_t num_counters = 0;
-  int* sched = nullptr;       // [0] work-queue head, [1] exited CTAs (both self-resetting)
+  int* sched = nullptr;       // [0] work-queue head (self-resetting)
   int* err = nullptr;         // device error word
   int num_sms = 0;
 };
