@@ -359,6 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[c / 2] = pack_bf16(e0, e1);
       }
       l += lt;
+      // Last tile: P V of tile n - 2 must be done before P n - 1 is published.
+      // kPvDone is then one phase short of the end when the epilogue waits for
+      // the last phase; were both last P V done by then, a wait for the parity
+      // of phase n - 2 would alias the never-completing phase n.
+      if (i == n - 1 && i > 0) mbar_wait(bar(kPvDone), (i - 1) & 1, p.err);
 #pragma unroll
       for (int uq = 0; uq < 4; ++uq)
         *reinterpret_cast<uint4*>(p_row(pb) + ((uq ^ pswz) & 3) * 16) =
@@ -372,9 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------ epilogue ------------------------------
     if (n > 0) {
-      // P V of tile n - 3 is done (the last kPFree wait): kPvDone is at most
-      // two phases short of the end
-      if (n >= 2) mbar_wait(bar(kPvDone), (n - 2) & 1, p.err);
+      // P V of tile n - 2 is done (waited for above): kPvDone is at most one
+      // phase short of the end
       mbar_wait(bar(kPvDone), (n - 1) & 1, p.err);
       __syncwarp();
       tc::fence_after_sync();
