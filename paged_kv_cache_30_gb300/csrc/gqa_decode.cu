@@ -63,6 +63,7 @@ constexpr int kQBytes = kGqaGroup * kGqaHeadDim * 2;
 constexpr int kWbRow = 132;            // padded O row of the combine buffer (floats)
 constexpr int kWbFloats = kGqaGroup * kWbRow + 2 * kGqaGroup;  // O[8][132], m[8], l[8]
 constexpr int kMergeGroup = 16;        // splits merged by one CTA at the first level
+constexpr int kClaimTiles = 8;         // claim the next item this many tiles before the end
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct ItemDesc {
@@ -277,8 +278,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // that fall to producer `mine`: whole pages, alternating (an item's first
   // tile number `seq` is a multiple of TPP, so a page's tiles share a parity
   // of seq / TPP and every ring stage is refilled by one producer only).
+  // At page claim_at (if in range) it calls on_page() first: the first
+  // producer claims its next item there.
   auto stream_tiles = [&](const int32_t* bt_row, int kvh, int p0, int p1, uint32_t seq,
-                          uint32_t mine) {
+                          uint32_t mine, int claim_at, auto&& on_page) {
     for (int pb = p0; pb < p1; pb += 32) {
       const int cnt = min(32, p1 - pb);
       int blk = 0;
@@ -287,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (blk < 0 || blk >= p.num_blocks) atomicOr(p.err, DEVERR_BAD_BLOCK);
       }
       for (int i = 0; i < cnt; ++i) {
+        if (pb + i == claim_at) on_page();
         const int blk_i = __shfl_sync(0xffffffffu, blk, i);
 #pragma unroll
         for (int sub = 0; sub < TPP; ++sub) {
@@ -314,7 +318,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       __syncwarp();
       if (lane == 0) mbar_arrive(iempty_bar(slot));
       if (d.item < 0) break;
-      stream_tiles(p.bt + (long long)d.b * p.bt_sb, d.kvh, d.p0, d.p1, (uint32_t)d.seq_base, 1u);
+      stream_tiles(p.bt + (long long)d.b * p.bt_sb, d.kvh, d.p0, d.p1, (uint32_t)d.seq_base, 1u,
+                   -1, [] {});
     }
     return;
   }
@@ -323,19 +328,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // ============ first producer warp: the queue, descriptors, even tiles ============
     // The fetch that returns total_items + gridDim.x - 1 is the launch's last
     // (each CTA stops after its first index past the end): it resets the head.
+    // The next item is claimed only when the current one has kClaimTiles
+    // tiles left to issue (enough to hide the atomic): a claimed item waits
+    // for the current one to end, so claiming at its start would leave a CTA
+    // holding up to two items when the queue runs dry.
     const int last_fetch = total_items + (int)gridDim.x - 1;
-    if (lane == 0 && first_item == last_fetch) atomicExch(&p.sched[0], 0);
-    int next = __shfl_sync(0xffffffffu, first_item, 0);
+    int fetched = first_item;  // lane 0's claim, not yet examined
     uint32_t seq = 0;
     for (int it = 0;; ++it) {
-      const int item = next;
-      if (item < total_items) {
-        if (lane == 0) {
-          next = atomicAdd(&p.sched[0], 1);
-          if (next == last_fetch) atomicExch(&p.sched[0], 0);
-        }
-        next = __shfl_sync(0xffffffffu, next, 0);
-      }
+      const int item = __shfl_sync(0xffffffffu, fetched, 0);
+      if (lane == 0 && item == last_fetch) atomicExch(&p.sched[0], 0);
       const int slot = it % kItemSlots;
       if (lane == 0) mbar_wait(iempty_bar(slot), ((it / kItemSlots) & 1) ^ 1u, p.err);
       __syncwarp();
@@ -377,7 +379,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           bulk_load(qbuf + slot * kQBytes + h * kGqaHeadDim * 2, qrow + h * p.q_sh,
                     kGqaHeadDim * 2, ifull_bar(slot));
       }
-      stream_tiles(p.bt + (long long)b * p.bt_sb, kvh, p0, p1, seq, 0u);
+      const int claim_at = max(p0, p1 - kClaimTiles / TPP);
+      stream_tiles(p.bt + (long long)b * p.bt_sb, kvh, p0, p1, seq, 0u, claim_at, [&] {
+        if (lane == 0) fetched = atomicAdd(&p.sched[0], 1);
+      });
+      if (p1 <= p0 && lane == 0) fetched = atomicAdd(&p.sched[0], 1);  // an item of no pages
       seq += (uint32_t)((p1 - p0) * TPP);
     }
     if (lane == 0) {
