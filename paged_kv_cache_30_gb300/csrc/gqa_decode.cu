@@ -63,7 +63,7 @@ constexpr int kQBytes = kGqaGroup * kGqaHeadDim * 2;
 constexpr int kWbRow = 132;            // padded O row of the combine buffer (floats)
 constexpr int kWbFloats = kGqaGroup * kWbRow + 2 * kGqaGroup;  // O[8][132], m[8], l[8]
 constexpr int kMergeGroup = 16;        // splits merged by one CTA at the first level
-constexpr int kClaimTiles = 8;         // claim the next item this many tiles before the end
+constexpr int kClaimTiles = 4;         // claim the next item this many tiles before the end
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct ItemDesc {
@@ -379,7 +379,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           bulk_load(qbuf + slot * kQBytes + h * kGqaHeadDim * 2, qrow + h * p.q_sh,
                     kGqaHeadDim * 2, ifull_bar(slot));
       }
-      const int claim_at = max(p0, p1 - kClaimTiles / TPP);
+      // claim_at lies in [p0, p1) for any item with pages, so every item claims once
+      const int claim_at = max(p0, p1 - max(1, kClaimTiles / TPP));
       stream_tiles(p.bt + (long long)b * p.bt_sb, kvh, p0, p1, seq, 0u, claim_at, [&] {
         if (lane == 0) fetched = atomicAdd(&p.sched[0], 1);
       });
