@@ -348,7 +348,8 @@ PKV_API int pkv_mla_kv_append(const pkv_tensor* latent, const pkv_tensor* latent
  * pkv_check_errors -- read and clear the device error word of `device`
  * (synchronises the device).  *flags receives the OR of the bits raised since
  * the last check: 1 bad block-table entry, 2 seq_len longer than the block
- * table, 4 a pipeline wait gave up, 8 work items beyond the workspace.
+ * table, 4 a pipeline wait gave up, 8 work items beyond the workspace, 16 a
+ * CTA drew more work items than the launch has (the CTA stopped).
  * Returns PKV_OK when no bit was set, PKV_ERR_BAD_BLOCK_TABLE for bits 1|2,
  * PKV_ERR_CUDA otherwise (or on a failed CUDA call).
  */

@@ -341,8 +341,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int slot = it % kItemSlots;
       if (lane == 0) mbar_wait(iempty_bar(slot), ((it / kItemSlots) & 1) ^ 1u, p.err);
       __syncwarp();
-      if (item >= total_items) {
+      // no CTA can take more items than the launch has: the item loop is bounded
+      const bool runaway = it > total_items;
+      if (item >= total_items || runaway) {
         if (lane == 0) {
+          if (runaway) atomicOr(p.err, DEVERR_QUEUE);
           griddep_launch_dependents();  // the queue is empty: this CTA only drains now
           items[slot].item = -1;
           mbar_arrive(dfull_bar(slot));

@@ -18,6 +18,7 @@ enum : int {
   DEVERR_SEQ_TOO_LONG = 2,   // seq_len needs more pages than the block table holds
   DEVERR_WAIT_TIMEOUT = 4,   // a pipeline wait gave up (the kernel drained and returned)
   DEVERR_ITEM_OVERFLOW = 8,  // more work items than the workspace holds
+  DEVERR_QUEUE = 16,         // a CTA drew more items than the launch has (it stopped)
 };
 
 // Per-device workspace carved out of one allocation (see api.cpp).
