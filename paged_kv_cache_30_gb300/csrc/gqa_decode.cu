@@ -17,7 +17,9 @@
 //    from a global queue (an atomic head; every CTA fetches until it draws an
 //    index past the end, so the launch makes exactly items + CTAs fetches and
 //    the CTA that draws the last one resets the head to zero), so the launch
-//    shape depends only on the device and the batch.
+//    shape depends only on the device and the batch.  A CTA claims its next
+//    item only when the current one has a few tiles left to issue, so when the
+//    queue runs dry no CTA still holds an unstarted item.
 //  * The first producer warp takes items from the queue, writes each item's
 //    descriptor and bulk-copies its 8 query rows into a descriptor slot.  Both
 //    producer warps read block-table entries 32 at a time and stream the
