@@ -240,36 +240,43 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   // ---- prologue: the item list, identical in every CTA -------------------
   const int B = p.B;
-  int local_pages = 0;
-  for (int b = tid; b < B; b += kThreads) {
-    const int raw = __ldg(p.seq_lens + b);
-    if ((long long)raw > (long long)p.max_blocks * P) atomicOr(p.err, DEVERR_SEQ_TOO_LONG);
-    const int L = clamp_len<P>(p, b);
-    local_pages += (L + P - 1) / P - window_start(p, L) / P;
+  // With a split cap of 1, or a window that spans at most min_pages pages
+  // (no request then reaches two splits: chunk >= min_pages), item i is
+  // (request i / Hkv, kv head i % Hkv) and no scan is needed.  A window of W
+  // tokens touches at most (W + 2P - 2) / P pages.
+  const bool one_split = p.cap <= 1 || (p.window > 0 && (p.window + 2 * P - 2) / P <= p.min_pages);
+  int total_items = B * p.Hkv;
+  if (!one_split) {
+    int local_pages = 0;
+    for (int b = tid; b < B; b += kThreads) {
+      const int raw = __ldg(p.seq_lens + b);
+      if ((long long)raw > (long long)p.max_blocks * P) atomicOr(p.err, DEVERR_SEQ_TOO_LONG);
+      const int L = clamp_len<P>(p, b);
+      local_pages += (L + P - 1) / P - window_start(p, L) / P;
+    }
+    int total_pages;
+    block_exclusive_scan(local_pages, misc, &total_pages);
+    const long long total_ph = (long long)total_pages * p.Hkv;
+    int chunk = (int)((total_ph + p.target_items - 1) / p.target_items);
+    if (chunk < p.min_pages) chunk = p.min_pages;
+    const int per = (B + kThreads - 1) / kThreads;
+    const int b0 = tid * per;
+    int my_items = 0;
+    for (int i = 0; i < per && b0 + i < B; ++i) {
+      const int L = clamp_len<P>(p, b0 + i);
+      const int n = (L + P - 1) / P - window_start(p, L) / P;
+      const int s = max(1, min(p.cap, (n + chunk - 1) / chunk));
+      my_items += s * p.Hkv;
+    }
+    int run = block_exclusive_scan(my_items, misc, &total_items);
+    for (int i = 0; i < per && b0 + i < B; ++i) {
+      prefix[b0 + i] = run;
+      const int L = clamp_len<P>(p, b0 + i);
+      const int n = (L + P - 1) / P - window_start(p, L) / P;
+      run += max(1, min(p.cap, (n + chunk - 1) / chunk)) * p.Hkv;
+    }
+    if (tid == 0) prefix[B] = total_items;
   }
-  int total_pages;
-  block_exclusive_scan(local_pages, misc, &total_pages);
-  const long long total_ph = (long long)total_pages * p.Hkv;
-  int chunk = (int)((total_ph + p.target_items - 1) / p.target_items);
-  if (chunk < p.min_pages) chunk = p.min_pages;
-  const int per = (B + kThreads - 1) / kThreads;
-  const int b0 = tid * per;
-  int my_items = 0;
-  for (int i = 0; i < per && b0 + i < B; ++i) {
-    const int L = clamp_len<P>(p, b0 + i);
-    const int n = (L + P - 1) / P - window_start(p, L) / P;
-    const int s = max(1, min(p.cap, (n + chunk - 1) / chunk));
-    my_items += s * p.Hkv;
-  }
-  int total_items;
-  int run = block_exclusive_scan(my_items, misc, &total_items);
-  for (int i = 0; i < per && b0 + i < B; ++i) {
-    prefix[b0 + i] = run;
-    const int L = clamp_len<P>(p, b0 + i);
-    const int n = (L + P - 1) / P - window_start(p, L) / P;
-    run += max(1, min(p.cap, (n + chunk - 1) / chunk)) * p.Hkv;
-  }
-  if (tid == 0) prefix[B] = total_items;
   if ((long long)total_items > p.max_items) {
     if (tid == 0) atomicOr(p.err, DEVERR_ITEM_OVERFLOW);
     total_items = (int)p.max_items;
@@ -355,15 +362,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         break;
       }
-      int lo = 0, hi = B - 1;  // request = last b with prefix[b] <= item
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+      int b, nsplit, kvh, split;
+      if (one_split) {
+        b = item / p.Hkv;
+        kvh = item - b * p.Hkv;
+        nsplit = 1;
+        split = 0;
+        // the check the scanning prologue makes, once per request
+        if (lane == 0 && kvh == 0 && (long long)__ldg(p.seq_lens + b) > (long long)p.max_blocks * P)
+          atomicOr(p.err, DEVERR_SEQ_TOO_LONG);
+      } else {
+        int lo = 0, hi = B - 1;  // request = last b with prefix[b] <= item
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        nsplit = (prefix[b + 1] - prefix[b]) / p.Hkv;
+        const int local = item - prefix[b];
+        kvh = local / nsplit;
+        split = local % nsplit;
       }
-      const int b = lo;
-      const int nsplit = (prefix[b + 1] - prefix[b]) / p.Hkv;
-      const int local = item - prefix[b];
-      const int kvh = local / nsplit, split = local % nsplit;
       const int L = clamp_len<P>(p, b);
       const int start_tok = window_start(p, L);
       const int sp = start_tok / P;

@@ -85,6 +85,9 @@ def test_tiny_gqa_config(seed):
     (6, 9, 1, 16, 1, 40, True, 0, 64),
     (7, 2, 2, 32, 1000, 5000, True, 1, 0),
     (8, 8, 1, 32, 31, 33, False, 32, 2),
+    (9, 5, 2, 16, 1, 2000, True, 0, 1),      # cap 1: one item per (request, kv head)
+    (10, 6, 1, 16, 1, 3000, True, 226, 0),   # widest window whose items never split at P 16
+    (11, 6, 1, 16, 1, 3000, True, 243, 0),   # one token wider: the scanning prologue
 ])
 def test_random_cases(seed, B, Hkv, P, Lmin, Lmax, sinks, window, cap):
     prob = W.gqa_problem(seed, B, 8 * Hkv, Hkv, P, "uniform", Lmin, Lmax, sinks=sinks,
@@ -274,13 +277,16 @@ def test_bad_block_table_entry_is_flagged_not_faulted():
     check(prob, what="after bad table")
 
 
-def test_seq_len_beyond_block_table_is_flagged():
+@pytest.mark.parametrize("window, cap", [(0, 0), (128, 0), (0, 1)])
+def test_seq_len_beyond_block_table_is_flagged(window, cap):
+    # (128, 0) and (0, 1): no request can split, so the kernel skips the
+    # scanning prologue and checks the lengths as it decodes each item
     prob = W.gqa_problem(22, 2, 8, 1, 16, "const", 64, 64, max_blocks=4)
     sl = prob.seq_lens.clone()
     sl[0] = 1000
     out = torch.empty_like(dev(prob.q))
     pkv.paged_decode_attn(dev(prob.q), dev(prob.kv_cache), dev(prob.block_table), sl.cuda(),
-                          None, 0, prob.scale, 16, 0, out, None)
+                          None, window, prob.scale, 16, cap, out, None)
     with pytest.raises(pkv.PkvError) as ei:
         pkv.check_errors(0)
     assert ei.value.code == -7
