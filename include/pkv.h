@@ -48,7 +48,12 @@
  *  - Calls that share a device's workspace must be ordered on one stream (as
  *    within one model forward).  When a call arrives on a different stream
  *    than the previous call on that device (and neither is being captured),
- *    the new stream first waits for the previous one.
+ *    the new stream first waits for the previous one: the library records an
+ *    event on the previous call's stream at that moment, so that stream must
+ *    still exist (destroy a stream only after another call on the device has
+ *    been made from a live stream, or after pkv_shutdown()).  No event is
+ *    recorded between calls on one stream, which keeps consecutive launches
+ *    overlapping (programmatic dependent launch).
  *  - The launch shape depends only on the device and the batch size, never on
  *    the sequence lengths or the block table, which the kernels read on the
  *    device: a captured graph stays valid when seq_lens and block_table change.
