@@ -7,7 +7,7 @@ import torch
 import oracle
 import paged_kv_cache_30_gb300 as pkv
 from paged_kv_cache_30_gb300 import workloads as W
-from tests.gpu_helpers import TOL_LSE, TOL_OUT, TOL_OUT_FP8, compare
+from tests.gpu_helpers import TOL_LSE, TOL_OUT, TOL_OUT_FP8, compare, within_bf16_reorder
 
 pytestmark = pytest.mark.gpu
 
@@ -110,23 +110,38 @@ def test_mla_degenerate_warmup_inputs():
             check(prob, cap, what=f"warmup qlen {qlen} cap {cap}")
 
 
+# Between two split counts of one MLA call.  Measured on GB300 (this test's
+# problem and the B=32 qlen-4 workload, caps 1, 2, 5, 8, 16 against cap 1):
+# outputs differ by at most one bf16 ulp of the output (7.8e-3 at |out| = 1.08,
+# where an ulp is 2^-7; 99th percentile 4.9e-4) and lse by 9.5e-7.  The fp32
+# results of two split counts differ only by accumulation order (~1e-6
+# relative) and each is rounded once to bf16, so where they straddle a rounding
+# boundary they land one ulp apart: the bound is relative to the output's
+# magnitude, not an absolute 2e-3 (GQA outputs stay below ~0.25, where one ulp
+# is at most 2^-10).
+MLA_INV_ULPS = 1.0
+MLA_INV_LSE = 1e-5
+
+
+def check_split_invariance(outs, what):
+    o1, l1 = outs[0]
+    for i, (out, lse) in enumerate(outs[1:], 1):
+        assert within_bf16_reorder(out, o1, ulps=MLA_INV_ULPS, floor=1e-4), \
+            f"{what} #{i}: out more than {MLA_INV_ULPS} bf16 ulp from cap 1"
+        fin = np.isfinite(l1)
+        assert np.array_equal(fin, np.isfinite(lse))
+        d_lse = float(np.max(np.abs(lse[fin] - l1[fin]))) if fin.any() else 0.0
+        assert d_lse <= MLA_INV_LSE, f"{what} #{i}: lse differs by {d_lse:.3g} from cap 1"
+
+
 def test_mla_split_count_invariance():
     prob = mla_case(9, [6000, 3333], 4, 16, real=[5998, 3333])
-    outs = []
-    for cap in (1, 2, 5, 8, 16):
-        outs.append(run_mla(prob, cap))
+    caps = (1, 2, 5, 8, 16)
+    outs = [run_mla(prob, cap) for cap in caps]
     ref_out, ref_lse = oracle_mla(prob)
-    for cap, (out, lse) in zip((1, 2, 5, 8, 16), outs):
+    for cap, (out, lse) in zip(caps, outs):
         compare(out, lse, ref_out.reshape(out.shape), ref_lse.reshape(lse.shape), what="inv")
-        # Another split count changes more than the accumulation order: each
-        # split rounds P to bf16 against its own reference max, so the outputs
-        # of two split counts differ by up to twice the P-rounding error
-        # (2 x 2^-9 x max|V| ~ 2e-2 here) -- the stated output tolerance.
-        # lse comes from fp32 sums and stays within 3e-4.
-        d_out = float(np.max(np.abs(out - outs[0][0])))
-        d_lse = float(np.max(np.abs(lse - outs[0][1])))
-        assert d_out <= TOL_OUT, f"cap {cap}: out differs by {d_out:.3g} from cap 1"
-        assert d_lse <= 3e-4, f"cap {cap}: lse differs by {d_lse:.3g} from cap 1"
+    check_split_invariance(outs, "mla inv")
 
 
 def test_mla_repeated_calls_are_bitwise_identical():
@@ -140,12 +155,20 @@ def test_mla_repeated_calls_are_bitwise_identical():
     assert pkv.check_counters(0) == 0
 
 
-def test_mla_verify_b32_full_size_sampled_rows():
-    """B=32, qlen=4, H=128, L ~ U[512, 8192], L_real = L - U[0,3], cap 8: the
-    whole launch on the GPU, 1024 sampled rows against the oracle."""
+def test_mla_verify_b32_full_size_every_row():
+    """B=32, qlen=4, H=128, L ~ U[512, 8192], L_real = L - U[0,3]: every
+    (row, head) against the oracle in the benchmark's launch configuration
+    (cap 8), and at caps 1 and 2 (split-count invariance)."""
     prob = W.mla_verify(0)
-    rows = np.random.default_rng(1).choice(32 * 4 * 128, size=1024, replace=False)
-    check(prob, rows=rows, what="mla config b32 q4")
+    R, H, _ = prob.q.shape
+    ref_out, ref_lse = oracle_mla(prob)
+    outs = []
+    for cap in (1, 2, 8):
+        out, lse = run_mla(prob, cap)
+        compare(out, lse, ref_out.reshape(R, H, 512), ref_lse.reshape(R, H),
+                what=f"mla config b32 q4 cap {cap}")
+        outs.append((out, lse))
+    check_split_invariance(outs, "mla b32 q4")
 
 
 @pytest.mark.parametrize("seed,L,qlen,real,k_scale,cap", [
@@ -163,12 +186,10 @@ def test_mla_fp8_small_cases(seed, L, qlen, real, k_scale, cap):
     check(prob, what=f"fp8 case {seed}")
 
 
-def test_mla_fp8_b128_full_size_sampled_rows():
+def test_mla_fp8_b128_full_size_every_row():
     """B=128, qlen=1, H=128, e4m3 latent cache holding N(0,1)/k_scale, k_scale
-    0.05, log-uniform L in [1, 32768], cap 16: 1024 sampled rows."""
-    prob = W.mla_fp8(0)
-    rows = np.random.default_rng(2).choice(128 * 128, size=1024, replace=False)
-    check(prob, rows=rows, what="mla fp8 b128")
+    0.05, log-uniform L in [1, 32768], cap 16: every (row, head)."""
+    check(W.mla_fp8(0), what="mla fp8 b128")
 
 
 def test_mla_request_order_paths():
