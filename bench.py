@@ -283,16 +283,32 @@ def _tiny(dev, flush, steps, tiny, gqa_entry):
     return d
 
 
-def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
+def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None, sampler=None):
     """Every other workload of the pages' problem, timed the same way (inputs
     resident, L2 flushed between calls by L2Flush, CUDA events): the tiny decode batch,
     the 131072-token long context at B=1 and B=8 across split caps, the two
     MLA verify workloads (bf16 and FP8 latent caches) and the paged KV append
-    that precedes a decode or verify call."""
+    that precedes a decode or verify call.  With a running ClockSampler, each
+    entry gets the clock record of its own timed calls."""
     import torch
     import paged_kv_cache_30_gb300 as pkv
     from paged_kv_cache_30_gb300 import workloads as W
     res = {}
+    t_mark = [time.time()]
+
+    def stamp(*names):
+        """Attach the clocks sampled since the last stamp to these entries."""
+        t_end = time.time()
+        if sampler is not None:
+            c = sampler.summary(t_mark[0], t_end)
+            for n in names:
+                if isinstance(res.get(n), dict):
+                    res[n]["clocks"] = c
+        t_mark[0] = t_end
+
+    def start():
+        torch.cuda.synchronize()
+        t_mark[0] = time.time()
 
     def gqa_entry(prob, caps):
         t = dict(q=prob.q.to(dev), kv=prob.kv_cache.to(dev), bt=prob.block_table.to(dev),
@@ -315,12 +331,17 @@ def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
     want = (lambda k: only is None or k in only)
     # tiny decode batch: latency-bound, report calls/s eager and as CUDA-graph replay
     if want("tiny"):
-        res["tiny_gqa_b4"] = _tiny(dev, flush, steps, W.tiny_gqa(0), gqa_entry)
+        tiny = W.tiny_gqa(0)
+        start()
+        res["tiny_gqa_b4"] = _tiny(dev, flush, steps, tiny, gqa_entry)
+        stamp("tiny_gqa_b4")
     for B in (1, 8):
         if not want(f"long{B}"):
             continue
         prob = W.long_context(0, B=B)
+        start()
         res[f"long_ctx_b{B}"], _ = gqa_entry(prob, [0, 1, 8, 32, 132])
+        stamp(f"long_ctx_b{B}")
         del prob
 
     for key, name, mk in (("mla", "mla_verify_b32_q4", W.mla_verify),
@@ -337,6 +358,7 @@ def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
         lse = torch.empty((tq.shape[0], 128), device=dev)
         fn = lambda: pkv.mla_verify_attn(tq, tc, tbt, tsl, trl, prob.qlen, prob.scale,
                                          prob.page_size, ks, out, lse, prob.num_kv_splits)
+        start()
         med, _ = time_events(fn, flush, steps)
         fl = mla_flops(prob)
         nbytes = prob.kv_bytes()
@@ -344,6 +366,7 @@ def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
                      "tensor_frac_of_measured_bf16": fl / (med * 1e-3) / 1e12 / peak_tf,
                      "GBps": nbytes / (med * 1e-3) / 1e9, "flops": fl, "kv_bytes": nbytes,
                      "cap": prob.num_kv_splits}
+        stamp(name)
         if key == "mla_fp8" and want("native"):
             # the same workload on the native-FP8 path: query quantised to e4m3
             # per (row, head) inside the timed call, S on kind::f8f6f4 MMAs
@@ -354,6 +377,7 @@ def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
                 pkv.mla_quantize_q(tq, q8, qs)
                 pkv.mla_verify_attn_fp8_native(q8, qs, tc, tbt, tsl, trl, prob.qlen, prob.scale,
                                                prob.page_size, ks, out, lse, prob.num_kv_splits)
+            start()
             med_n, _ = time_events(fn_native, flush, steps)
             res["mla_fp8_native_b128"] = {
                 "us": 1e3 * med_n, "TFLOPs": fl / (med_n * 1e-3) / 1e12,
@@ -362,6 +386,7 @@ def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
                 "cap": prob.num_kv_splits,
                 "note": "query quantised to e4m3 (an opt-in numerics change); the quantisation "
                         "kernel is inside the timed call"}
+            stamp("mla_fp8_native_b128")
             del q8, qs
         del tq, tc
     if want("append"):
@@ -373,6 +398,7 @@ def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
         v = W.normal((B, Hq // 8, 128), 92).to(dev)
         kv, bt, sl = prob.kv_cache.to(dev), prob.block_table.to(dev), prob.seq_lens.to(dev)
         fn = lambda: pkv.gqa_kv_append(k, v, kv, bt, sl, prob.page_size)
+        start()
         med, _ = time_events(fn, flush, steps)
         nbytes = 2 * int((prob.seq_lens > 0).sum()) * (Hq // 8) * 512  # read + written
         res["kv_append_flint_b64"] = {"us": 1e3 * med, "GBps": nbytes / (med * 1e-3) / 1e9,
@@ -381,11 +407,14 @@ def other_workloads(dev, flush, peak_hbm, peak_tf, steps, only=None):
         mp = W.mla_verify(0)
         lat = W.normal((mp.q.shape[0], 576), 93).to(dev)
         cache, mbt, msl = mp.latent_cache.to(dev), mp.block_table.to(dev), mp.seq_lens.to(dev)
+        stamp("kv_append_flint_b64")
         fn = lambda: pkv.mla_kv_append(lat, cache, mbt, msl, mp.qlen, mp.page_size)
+        start()
         med, _ = time_events(fn, flush, steps)
         nbytes = 2 * mp.q.shape[0] * 1152
         res["kv_append_mla_b32_q4"] = {"us": 1e3 * med, "GBps": nbytes / (med * 1e-3) / 1e9,
                                        "rows": int(mp.q.shape[0])}
+        stamp("kv_append_mla_b32_q4")
         del cache
     assert pkv.check_errors(dev.index or 0) == 0
     return res
@@ -564,8 +593,6 @@ def run_gpu(args, rank, world, local_rank):
         e[2].record(stream)
     barrier()
     t2 = time.time()
-    time.sleep(0.2)
-    sampler.stop()
     full_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
     step_ms_evented = statistics.mean(ev[s][0].elapsed_time(ev[s][2]) for s in range(args.steps))
     full_mean = statistics.mean(full_ms)
@@ -681,9 +708,13 @@ def run_gpu(args, rank, world, local_rank):
                          f"{threads} threads"}
 
     extra = None
-    if world == 1 and not args.no_extra:
-        extra = other_workloads(dev, flush, peak, measured_bf16_tflops(), args.extra_steps)
-
+    try:
+        if world == 1 and not args.no_extra:
+            extra = other_workloads(dev, flush, peak, measured_bf16_tflops(), args.extra_steps,
+                                    sampler=sampler)
+        time.sleep(0.2)
+    finally:
+        sampler.stop()
     clocks = sampler.summary(t0, t2)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -57,6 +57,14 @@
  *  - The launch shape depends only on the device and the batch size, never on
  *    the sequence lengths or the block table, which the kernels read on the
  *    device: a captured graph stays valid when seq_lens and block_table change.
+ *  - The call's device is the device holding its first tensor argument (q, or
+ *    the cache for the append calls): it must be the current device and the
+ *    stream's device, else PKV_ERR_INVALID_ARG.  (While the stream is being
+ *    captured these pointer queries are skipped and the current device is
+ *    used: a capture follows an eager call that has checked them.)  Outputs may not share memory
+ *    with any input or with each other (PKV_ERR_INVALID_ARG): the kernels read
+ *    the inputs of one request after writing the outputs of another.  A block
+ *    table of width W over pages of P tokens needs W x P < 2^31.
  *  - Data-dependent input errors that the host cannot see (a block-table entry
  *    outside the cache, a seq_len longer than the block table) never fault:
  *    the kernel clamps or zero-fills, raises a bit in the device error word and
@@ -142,13 +150,16 @@ PKV_API int pkv_init(int device, size_t workspace_bytes);
  *                head); 0 selects the library's cap; values above 256 act as
  *                256.  Each request uses as many splits as its own length
  *                warrants (at least 256 keys per split), at most this many.
- *   out          bf16 [B, Hq, 128] (may not alias q); last dim contiguous.
+ *   out          bf16 [B, Hq, 128]; last dim contiguous; shares no memory with
+ *                any input or with lse.
  *   lse          fp32 [B, Hq] or NULL.
  *   stream       cudaStream_t (NULL = legacy default stream).
  * B == 0 returns PKV_OK without launching.
- * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED (head dim != 128, Hq != 8*Hkv,
- * P not in {16, 32}, B > 2048), PKV_ERR_ALIGNMENT, PKV_ERR_WORKSPACE (B * Hkv *
- * cap partials do not fit), PKV_ERR_CAPTURE, PKV_ERR_CUDA.
+ * Errors: PKV_ERR_INVALID_ARG (shapes, dtypes, overlapping outputs, q not on
+ * the current device or the stream's), PKV_ERR_UNSUPPORTED (head dim != 128,
+ * Hq != 8*Hkv, P not in {16, 32}, B > 2048), PKV_ERR_ALIGNMENT,
+ * PKV_ERR_WORKSPACE (B * Hkv * cap partials do not fit; a cap of 1 needs
+ * none), PKV_ERR_CAPTURE, PKV_ERR_CUDA.
  */
 PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cache,
                                   const pkv_tensor* block_table, const pkv_tensor* seq_lens,
@@ -161,19 +172,21 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
  * library never allocates.  The pages have no counterpart: this entry point
  * exists for callers that cannot let a library call cudaMalloc, e.g. a serving
  * engine that reserves all of HBM for its own KV-cache pool and treats any
- * other device allocation as an out-of-memory risk, a framework whose memory
- * manager must own every device buffer, or code that runs while a stream
- * capture forbids allocation.
+ * other device allocation as an out-of-memory risk, or a framework whose
+ * memory manager must own every device buffer.
  *
  * Arguments, layouts, results and error codes are those of
- * pkv_paged_decode_attn.  The split partials, arrival counters and work-queue
- * words live in one file-scope __device__ array of about 8.2 MiB that every
- * GPU loading the library holds until the process exits.  Limits: batch x kv
- * heads <= 4096 and batch x kv heads x splits <= 2048 (the split cap is chosen
- * to fit when num_kv_splits is 0); larger calls return PKV_ERR_WORKSPACE and
- * launch nothing.  The call allocates nothing: no cudaMalloc, cudaFree or
- * allocating library routine, and it never touches the workspace of
- * pkv_init.  Each call clears the array's counters with cudaMemsetAsync on
+ * pkv_paged_decode_attn, and so is the launch shape (split cap, grid, items
+ * per CTA), computed on this array's limits.  The split partials, arrival
+ * counters, work-queue words and device error word live in one file-scope
+ * __device__ array of about 8.2 MiB that every GPU loading the library holds
+ * until the process exits.  Limits: batch x kv heads <= 4096, and batch x kv
+ * heads x splits <= 2048 whenever a request may split (cap > 1; the cap is
+ * chosen to fit when num_kv_splits is 0, falling to 1 above 1024 pairs);
+ * larger calls return PKV_ERR_WORKSPACE and launch nothing.  The call
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library routine,
+ * and it never touches the workspace of pkv_init.  Each call clears the
+ * array's counters, queue words and error word with cudaMemsetAsync on
  * `stream` before its launch.
  *   - The first call on a device looks up the array's device address on that
  *     device (cudaGetSymbolAddress); make that first call before any stream
@@ -181,9 +194,15 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
  *   - Every call shares the one array: calls whose kernels may overlap on the
  *     GPU (different streams without ordering, different threads) race and
  *     give wrong results.  Order them on one stream.
- *   - Device-side input errors (bad block-table entries) are clamped or
- *     zero-filled as on the allocating path but are not reported:
- *     pkv_check_errors does not see this path.
+ *   - Device-side errors of the last call are kept in the array's error word
+ *     until the next call clears it; pkv_check_errors(device) reads (and
+ *     clears) it together with the workspace's word: bit 1 a block-table
+ *     entry outside the cache (the tile reads as zeros), bit 2 a seq_len
+ *     longer than the block table (clamped), bit 4 a pipeline wait that gave
+ *     up (that CTA drained; its outputs are wrong), bit 8 more work items
+ *     than the array holds (the excess was dropped), bit 16 a CTA that drew
+ *     more items than the launch has (it stopped).  Any bit other than 1 and
+ *     2 means the outputs of that call are not to be trusted.
  */
 PKV_API int pkv_paged_decode_attn_noalloc(const pkv_tensor* q, const pkv_tensor* kv_cache,
                                           const pkv_tensor* block_table,
@@ -284,6 +303,11 @@ PKV_API int pkv_mla_verify_attn_fp8_native(const pkv_tensor* q8, const pkv_tenso
  *   row blocks = cdiv(qlen * num_heads, block_h).
  * Returns the cap (>= 1), or PKV_ERR_INVALID_ARG for non-positive sm_count,
  * block_h, qlen or num_heads, or a negative occupancy.
+ * Advisory: the attention calls do not call it.  A caller may pass its result
+ * as num_kv_splits; with num_kv_splits == 0 the library picks its own cap, and
+ * in either case each request's actual split count is chosen on the device
+ * from the lengths (GQA: about four work items per CTA, at least 256 keys per
+ * split; MLA: at least 4096 keys per split).
  */
 PKV_API int pkv_num_kv_splits(int max_seq_len, int batch, int qlen, int num_heads, int sm_count,
                               int block_h, double occupancy, int min_work_per_split,
@@ -350,9 +374,10 @@ PKV_API int pkv_mla_kv_append(const pkv_tensor* latent, const pkv_tensor* latent
                               int page_size, const pkv_tensor* k_scale, void* stream);
 
 /*
- * pkv_check_errors -- read and clear the device error word of `device`
- * (synchronises the device).  *flags receives the OR of the bits raised since
- * the last check: 1 bad block-table entry, 2 seq_len longer than the block
+ * pkv_check_errors -- read and clear the device error words of `device` (the
+ * workspace's, and that of pkv_paged_decode_attn_noalloc's static array once
+ * a call has set it up; synchronises the device).  *flags receives the OR of
+ * the bits raised since the last check: 1 bad block-table entry, 2 seq_len longer than the block
  * table, 4 a pipeline wait gave up, 8 work items beyond the workspace, 16 a
  * CTA drew more work items than the launch has (the CTA stopped).
  * Returns PKV_OK when no bit was set, PKV_ERR_BAD_BLOCK_TABLE for bits 1|2,

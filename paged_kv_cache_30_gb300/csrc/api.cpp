@@ -13,7 +13,9 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <initializer_list>
 #include <string>
+#include <utility>
 
 #include "pkv_internal.h"
 
@@ -92,15 +94,13 @@ int init_locked(int device, size_t partial_bytes) {
   return PKV_OK;
 }
 
-// Workspace of the current device, allocating it on first use (refused while
-// the stream is being captured: allocation would not be part of the graph).
-int workspace_for(cudaStream_t stream, int* device, DeviceState** out, bool* capturing) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+// Workspace of `dev` (the device of the call's tensors, which the caller has
+// checked is current), allocating it on first use (refused while the stream
+// is being captured: allocation would not be part of the graph).
+int workspace_for(int dev, cudaStream_t stream, DeviceState** out, bool* capturing) {
   if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device %d", dev);
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  e = cudaStreamIsCapturing(stream, &cs);
+  cudaError_t e = cudaStreamIsCapturing(stream, &cs);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
   *capturing = cs != cudaStreamCaptureStatusNone;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -112,7 +112,6 @@ int workspace_for(cudaStream_t stream, int* device, DeviceState** out, bool* cap
     const int rc = init_locked(dev, 0);
     if (rc != PKV_OK) return rc;
   }
-  *device = dev;
   *out = &g_dev[dev];
   return PKV_OK;
 }
@@ -145,6 +144,95 @@ int check_tensor(const pkv_tensor* t, const char* name, int dtype, int ndim) {
   for (int i = 0; i < ndim; ++i)
     if (t->shape[i] < 0 || t->stride[i] < 0)
       return fail(PKV_ERR_INVALID_ARG, "%s has a negative size or stride", name);
+  return PKV_OK;
+}
+
+int elem_bytes(int dtype) {
+  switch (dtype) {
+    case PKV_DTYPE_BF16: return 2;
+    case PKV_DTYPE_F32: return 4;
+    case PKV_DTYPE_I32: return 4;
+    case PKV_DTYPE_FP8_E4M3: return 1;
+    default: return 1;
+  }
+}
+
+// Byte range [lo, hi) a strided view spans (empty when any size is 0).
+void byte_span(const pkv_tensor* t, uintptr_t* lo, uintptr_t* hi) {
+  *lo = *hi = reinterpret_cast<uintptr_t>(t->data);
+  int64_t last = 0;
+  for (int i = 0; i < t->ndim; ++i) {
+    if (t->shape[i] == 0) return;
+    last += (t->shape[i] - 1) * t->stride[i];
+  }
+  *hi = *lo + uintptr_t((last + 1) * elem_bytes(t->dtype));
+}
+
+// True when two views share any byte.
+bool overlaps(const pkv_tensor* a, const pkv_tensor* b) {
+  if (!a || !b) return false;
+  uintptr_t a0, a1, b0, b1;
+  byte_span(a, &a0, &a1);
+  byte_span(b, &b0, &b1);
+  return a0 < a1 && b0 < b1 && a0 < b1 && b0 < a1;
+}
+
+// Outputs may not share memory with any input or with each other: the kernels
+// read inputs of one request after writing outputs of another.
+int check_no_overlap(std::initializer_list<std::pair<const pkv_tensor*, const char*>> outputs,
+                     std::initializer_list<std::pair<const pkv_tensor*, const char*>> inputs) {
+  for (auto o = outputs.begin(); o != outputs.end(); ++o) {
+    for (const auto& i : inputs)
+      if (overlaps(o->first, i.first))
+        return fail(PKV_ERR_INVALID_ARG, "%s overlaps %s", o->second, i.second);
+    for (auto o2 = o + 1; o2 != outputs.end(); ++o2)
+      if (overlaps(o->first, o2->first))
+        return fail(PKV_ERR_INVALID_ARG, "%s overlaps %s", o->second, o2->second);
+  }
+  return PKV_OK;
+}
+
+// Requests hold at most max_blocks x page_size keys; the kernels keep that
+// product in 32-bit integers.
+int check_table_width(const pkv_tensor* block_table, int page_size) {
+  if (block_table->shape[1] < 1 || block_table->shape[1] * int64_t(page_size) >= (int64_t(1) << 31))
+    return fail(PKV_ERR_INVALID_ARG, "block_table width %lld x page_size %d must be in [1, 2^31)",
+                (long long)block_table->shape[1], page_size);
+  return PKV_OK;
+}
+
+// The device whose memory holds `t` (the call's device): it must be the
+// current device and the device of `stream`.  While `stream` is being
+// captured the pointer and stream queries are not made (they would end the
+// capture); the call's device is then the current one.
+int device_of(const pkv_tensor* t, const char* name, cudaStream_t stream, int* device) {
+  int cur = 0;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cs != cudaStreamCaptureStatusNone) {
+    if (cur < 0 || cur >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device %d", cur);
+    *device = cur;
+    return PKV_OK;
+  }
+  cudaPointerAttributes a;
+  e = cudaPointerGetAttributes(&a, t->data);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+    return fail(PKV_ERR_INVALID_ARG, "%s is not device memory", name);
+  const int dev = a.type == cudaMemoryTypeDevice ? a.device : cur;
+  if (dev != cur)
+    return fail(PKV_ERR_INVALID_ARG, "%s is on device %d but device %d is current", name, dev, cur);
+  int sdev = 0;
+  e = cudaStreamGetDevice(stream, &sdev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetDevice");
+  if (sdev != dev)
+    return fail(PKV_ERR_INVALID_ARG, "the stream belongs to device %d, %s to device %d", sdev, name,
+                dev);
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device %d", dev);
+  *device = dev;
   return PKV_OK;
 }
 
@@ -245,16 +333,22 @@ PKV_API int pkv_check_errors(int device, int32_t* flags) {
   if (!flags) return fail(PKV_ERR_INVALID_ARG, "flags is NULL");
   *flags = 0;
   if (device < 0 || device >= kMaxDevices) return fail(PKV_ERR_INVALID_ARG, "device %d", device);
+  // the error word of pkv_paged_decode_attn_noalloc's static scratch, if set up
+  int* noalloc_err = pkv::noalloc_error_word(device);
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState& st = g_dev[device];
-  if (!st.ws.base) return PKV_OK;
+  if (!st.ws.base && !noalloc_err) return PKV_OK;
   int prev = 0;
   cudaGetDevice(&prev);
   cudaSetDevice(device);
-  int32_t v = 0;
+  int32_t v = 0, w = 0;
   cudaError_t e = cudaDeviceSynchronize();
-  if (e == cudaSuccess) e = cudaMemcpy(&v, st.ws.err, 4, cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess) e = cudaMemset(st.ws.err, 0, 4);
+  for (int* word : {static_cast<int*>(st.ws.err), noalloc_err}) {
+    if (!word || e != cudaSuccess) continue;
+    e = cudaMemcpy(&w, word, 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(word, 0, 4);
+    v |= w;
+  }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   cudaSetDevice(prev);
   if (e != cudaSuccess) return cuda_fail(e, "pkv_check_errors");
@@ -343,122 +437,26 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
                                   const pkv_tensor* sinks, int window, float scale,
                                   int page_size, int num_kv_splits, const pkv_tensor* out,
                                   const pkv_tensor* lse, void* stream_ptr) {
-  int rc;
-  if ((rc = check_tensor(q, "q", PKV_DTYPE_BF16, 3))) return rc;
-  if ((rc = check_tensor(kv_cache, "kv_cache", PKV_DTYPE_BF16, 4))) return rc;
-  if ((rc = check_tensor(block_table, "block_table", PKV_DTYPE_I32, 2))) return rc;
-  if ((rc = check_tensor(seq_lens, "seq_lens", PKV_DTYPE_I32, 1))) return rc;
-  if ((rc = check_tensor(out, "out", PKV_DTYPE_BF16, 3))) return rc;
-  if (sinks && (rc = check_tensor(sinks, "sinks", PKV_DTYPE_F32, 1))) return rc;
-  if (lse && (rc = check_tensor(lse, "lse", PKV_DTYPE_F32, 2))) return rc;
-
-  const int64_t B = q->shape[0], Hq = q->shape[1], D = q->shape[2];
-  const int64_t nb = kv_cache->shape[0], Hkv = kv_cache->shape[1];
-  if (D != pkv::kGqaHeadDim)
-    return fail(PKV_ERR_UNSUPPORTED, "head_dim %lld (only 128 is built)", (long long)D);
-  if (kv_cache->shape[3] != 2 * D)
-    return fail(PKV_ERR_INVALID_ARG, "kv_cache last dim %lld, expected [K | V] = 256",
-                (long long)kv_cache->shape[3]);
-  if (Hkv <= 0 || Hq != pkv::kGqaGroup * Hkv)
-    return fail(PKV_ERR_UNSUPPORTED, "num_q_heads %lld must be 8 x num_kv_heads %lld",
-                (long long)Hq, (long long)Hkv);
-  if (page_size != 16 && page_size != 32)
-    return fail(PKV_ERR_UNSUPPORTED, "page_size %d (16 and 32 are built)", page_size);
-  if (kv_cache->shape[2] != page_size)
-    return fail(PKV_ERR_INVALID_ARG, "kv_cache.shape[2] %lld != page_size %d",
-                (long long)kv_cache->shape[2], page_size);
-  if (nb < 1 || nb >= (int64_t(1) << 31))
-    return fail(PKV_ERR_INVALID_ARG, "num_blocks %lld", (long long)nb);
-  if (block_table->shape[0] != B || seq_lens->shape[0] != B)
-    return fail(PKV_ERR_INVALID_ARG, "block_table / seq_lens batch mismatch");
-  if (out->shape[0] != B || out->shape[1] != Hq || out->shape[2] != D)
-    return fail(PKV_ERR_INVALID_ARG, "out shape mismatch");
-  if (sinks && sinks->shape[0] != Hq) return fail(PKV_ERR_INVALID_ARG, "sinks must be [Hq]");
-  if (sinks && sinks->shape[0] > 1 && sinks->stride[0] != 1)
-    return fail(PKV_ERR_INVALID_ARG, "sinks must be contiguous");
-  if (lse && (lse->shape[0] != B || lse->shape[1] != Hq))
-    return fail(PKV_ERR_INVALID_ARG, "lse must be [B, Hq]");
-  if (block_table->shape[1] < 1 || block_table->shape[1] > (int64_t(1) << 30))
-    return fail(PKV_ERR_INVALID_ARG, "block_table width %lld", (long long)block_table->shape[1]);
-  if (block_table->stride[1] != 1 && block_table->shape[1] > 1)
-    return fail(PKV_ERR_INVALID_ARG, "block_table rows must be contiguous");
-  if (seq_lens->stride[0] != 1 && B > 1)
-    return fail(PKV_ERR_INVALID_ARG, "seq_lens must be contiguous");
-  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
-  if (num_kv_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_splits < 0");
-  if (B > pkv::kGqaMaxBatch)
-    return fail(PKV_ERR_UNSUPPORTED, "batch %lld > %d", (long long)B, pkv::kGqaMaxBatch);
-  // layout rules of the HND page cache and 16-byte vector access
-  if (q->stride[2] != 1 || out->stride[2] != 1 || kv_cache->stride[3] != 1 ||
-      kv_cache->stride[2] != 2 * D)
-    return fail(PKV_ERR_INVALID_ARG, "q/out last dim and kv_cache rows must be contiguous");
-  if (q->stride[0] % 8 || q->stride[1] % 8 || out->stride[0] % 8 || out->stride[1] % 8 ||
-      kv_cache->stride[0] % 8 || kv_cache->stride[1] % 8)
-    return fail(PKV_ERR_ALIGNMENT, "strides of q, out and kv_cache must be multiples of 8");
-  if (!aligned16(q->data) || !aligned16(out->data) || !aligned16(kv_cache->data))
-    return fail(PKV_ERR_ALIGNMENT, "q, out and kv_cache must be 16-byte aligned");
-  if (B == 0) return PKV_OK;
-
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  int dev = 0;
+  pkv::GqaCall call;
+  int rc = pkv::prepare_gqa_call(q, kv_cache, block_table, seq_lens, sinks, window, scale,
+                                 page_size, num_kv_splits, out, lse, stream, &call);
+  if (rc != PKV_OK || call.pairs == 0) return rc;
   DeviceState* st = nullptr;
   bool capturing = false;
-  if ((rc = workspace_for(stream, &dev, &st, &capturing))) return rc;
+  if ((rc = workspace_for(call.device, stream, &st, &capturing))) return rc;
   const pkv::Workspace& ws = st->ws;
-
+  // partial slots: bounded by the partial bytes and by the split-group counters
   const int64_t item_bytes = int64_t(pkv::kGqaPartialFloats + pkv::kGqaMlFloats) * 4;
   const int64_t max_items =
       std::min<int64_t>(int64_t(ws.partial_bytes) / item_bytes, ws.num_counters - pkv::kTopCounters);
-  const int64_t bh = B * Hkv;
-  if (bh > pkv::kTopCounters)
-    return fail(PKV_ERR_WORKSPACE, "%lld (request, kv head) pairs exceed %lld counters",
-                (long long)bh, (long long)pkv::kTopCounters);
-  // At most 256 splits per (request, kv head): the merge runs in at most two
-  // levels of at most 16 partials each.
-  int64_t cap = num_kv_splits == 0 ? max_items / bh : num_kv_splits;
-  if (cap > 256) cap = 256;
-  if (cap < 1) cap = 1;
-  if (bh * cap > max_items)
-    return fail(PKV_ERR_WORKSPACE, "workspace holds %lld split partials, %lld x %lld needed",
-                (long long)max_items, (long long)bh, (long long)cap);
-
-  EncodeTiledFn encode = nullptr;
-  if ((rc = get_encoder(&encode))) return rc;
-  CUtensorMap map;
-  if ((rc = encode_gqa_kv_map(encode, kv_cache, page_size, &map))) return rc;
-
-  pkv::GqaParams p;
-  std::memset(&p, 0, sizeof p);
-  p.q = static_cast<const uint16_t*>(q->data);
-  p.q_sb = q->stride[0];
-  p.q_sh = q->stride[1];
-  p.bt = static_cast<const int32_t*>(block_table->data);
-  p.bt_sb = block_table->stride[0];
-  p.max_blocks = int(block_table->shape[1]);
-  p.num_blocks = int(nb);
-  p.seq_lens = static_cast<const int32_t*>(seq_lens->data);
-  p.sinks = sinks ? static_cast<const float*>(sinks->data) : nullptr;
-  p.out = static_cast<uint16_t*>(out->data);
-  p.o_sb = out->stride[0];
-  p.o_sh = out->stride[1];
-  p.lse = lse ? static_cast<float*>(lse->data) : nullptr;
-  p.lse_sb = lse ? lse->stride[0] : 0;
-  p.lse_sh = lse ? lse->stride[1] : 0;
-  p.B = int(B);
-  p.Hkv = int(Hkv);
-  p.window = window;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.scale = scale;
-  p.cap = int(cap);
-  p.min_pages = 256 / page_size;  // a split streams at least 256 tokens (128 KB per kv head)
-  const int64_t grid64 = std::min<int64_t>(int64_t(ws.num_sms) * pkv::gqa_ctas_per_sm(), bh * cap);
-  const int grid = int(grid64 < 1 ? 1 : grid64);
-  // About four items per CTA (A/B on the Flint batch: best of 2..24), but no
-  // more than 16 per (request, kv head) while that still gives every CTA one:
-  // a few long requests then stream fewer, larger splits, each merged in a
-  // single 16-way level (one 131072-token request, auto cap, on GB300:
-  // 118.7 -> 106.5 us; eight of them 632.8 -> 627.4 us).
-  p.target_items = int(std::max<int64_t>(grid, std::min<int64_t>(int64_t(grid) * 4, bh * 16)));
+  pkv::GqaShape shape;
+  if ((rc = pkv::gqa_launch_shape(call.pairs, call.cap_req, max_items, pkv::kTopCounters,
+                                  ws.num_sms, &shape)))
+    return rc;
+  pkv::GqaParams& p = call.p;
+  p.cap = shape.cap;
+  p.target_items = shape.target_items;
   p.part_o = ws.partials;
   p.part_ml = ws.partials + max_items * pkv::kGqaPartialFloats;
   p.max_items = max_items;
@@ -466,9 +464,8 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
   p.group_counters = ws.counters + pkv::kTopCounters;
   p.sched = ws.sched;
   p.err = ws.err;
-
   if ((rc = order_streams(st, stream, capturing))) return rc;
-  const cudaError_t e = pkv::launch_gqa_decode(p, map, page_size, grid, stream);
+  const cudaError_t e = pkv::launch_gqa_decode(p, call.map, page_size, shape.grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "gqa decode launch");
   return PKV_OK;
 }
@@ -564,13 +561,21 @@ static int mla_verify_impl(const pkv_tensor* q, const pkv_tensor* q8, const pkv_
     return fail(PKV_ERR_ALIGNMENT, "q and out must be 16-byte aligned with strides %% 8 == 0");
   if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
   if (num_kv_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_splits < 0");
+  if ((rc = check_table_width(block_table, page_size))) return rc;
+  if ((rc = check_no_overlap({{out, "out"}, {lse, "lse"}},
+                             {{q, native ? "q8" : "q"}, {q_scale, "q_scale"},
+                              {latent_cache, "latent_cache"}, {block_table, "block_table"},
+                              {seq_lens, "seq_lens"}, {real_seq_lens, "real_seq_lens"},
+                              {k_scale, "k_scale"}})))
+    return rc;
   if (B == 0) return PKV_OK;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   int dev = 0;
+  if ((rc = device_of(q, native ? "q8" : "q", stream, &dev))) return rc;
   DeviceState* st = nullptr;
   bool capturing = false;
-  if ((rc = workspace_for(stream, &dev, &st, &capturing))) return rc;
+  if ((rc = workspace_for(dev, stream, &st, &capturing))) return rc;
   const pkv::Workspace& ws = st->ws;
   // splits: at most 16 per (request, token, half); the device uses fewer for
   // short requests (at least 4096 keys per split)
@@ -731,11 +736,13 @@ PKV_API int pkv_mla_quantize_q(const pkv_tensor* q, const pkv_tensor* q8,
   if (R == 0) return PKV_OK;
   if (R * H >= (int64_t(1) << 31))
     return fail(PKV_ERR_INVALID_ARG, "%lld (row, head) pairs", (long long)(R * H));
+  if ((rc = check_no_overlap({{q8, "q8"}, {q_scale, "q_scale"}}, {{q, "q"}}))) return rc;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   int dev = 0;
+  if ((rc = device_of(q, "q", stream, &dev))) return rc;
   DeviceState* st = nullptr;
   bool capturing = false;
-  if ((rc = workspace_for(stream, &dev, &st, &capturing))) return rc;
+  if ((rc = workspace_for(dev, stream, &st, &capturing))) return rc;
   pkv::QuantParams p;
   p.q = static_cast<const uint16_t*>(q->data);
   p.q_sr = q->stride[0];
@@ -792,12 +799,18 @@ PKV_API int pkv_gqa_kv_append(const pkv_tensor* k, const pkv_tensor* v, const pk
     return fail(PKV_ERR_ALIGNMENT, "strides of k, v and kv_cache must be multiples of 8");
   if (!aligned16(k->data) || !aligned16(v->data) || !aligned16(kv_cache->data))
     return fail(PKV_ERR_ALIGNMENT, "k, v and kv_cache must be 16-byte aligned");
+  if ((rc = check_table_width(block_table, page_size))) return rc;
+  if ((rc = check_no_overlap({{kv_cache, "kv_cache"}},
+                             {{k, "k"}, {v, "v"}, {block_table, "block_table"},
+                              {seq_lens, "seq_lens"}})))
+    return rc;
   if (B == 0) return PKV_OK;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   int dev = 0;
+  if ((rc = device_of(kv_cache, "kv_cache", stream, &dev))) return rc;
   DeviceState* st = nullptr;
   bool capturing = false;
-  if ((rc = workspace_for(stream, &dev, &st, &capturing))) return rc;
+  if ((rc = workspace_for(dev, stream, &st, &capturing))) return rc;
   pkv::AppendParams p;
   std::memset(&p, 0, sizeof p);
   p.k = static_cast<const uint16_t*>(k->data);
@@ -881,12 +894,18 @@ PKV_API int pkv_mla_kv_append(const pkv_tensor* latent, const pkv_tensor* latent
   if (seq_lens->stride[0] != 1 && B > 1)
     return fail(PKV_ERR_INVALID_ARG, "seq_lens must be contiguous");
   if (R >= (int64_t(1) << 31)) return fail(PKV_ERR_UNSUPPORTED, "too many latent rows");
+  if ((rc = check_table_width(block_table, page_size))) return rc;
+  if ((rc = check_no_overlap({{latent_cache, "latent_cache"}},
+                             {{latent, "latent"}, {block_table, "block_table"},
+                              {seq_lens, "seq_lens"}, {k_scale, "k_scale"}})))
+    return rc;
   if (B == 0) return PKV_OK;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   int dev = 0;
+  if ((rc = device_of(latent_cache, "latent_cache", stream, &dev))) return rc;
   DeviceState* st = nullptr;
   bool capturing = false;
-  if ((rc = workspace_for(stream, &dev, &st, &capturing))) return rc;
+  if ((rc = workspace_for(dev, stream, &st, &capturing))) return rc;
   pkv::AppendParams p;
   std::memset(&p, 0, sizeof p);
   p.k = static_cast<const uint16_t*>(latent->data);
@@ -925,7 +944,7 @@ int prepare_gqa_call(const pkv_tensor* q, const pkv_tensor* kv_cache,
                      const pkv_tensor* block_table, const pkv_tensor* seq_lens,
                      const pkv_tensor* sinks, int window, float scale, int page_size,
                      int num_kv_splits, const pkv_tensor* out, const pkv_tensor* lse,
-                     GqaCall* call) {
+                     cudaStream_t stream, GqaCall* call) {
   int rc;
   if ((rc = check_tensor(q, "q", PKV_DTYPE_BF16, 3))) return rc;
   if ((rc = check_tensor(kv_cache, "kv_cache", PKV_DTYPE_BF16, 4))) return rc;
@@ -960,8 +979,7 @@ int prepare_gqa_call(const pkv_tensor* q, const pkv_tensor* kv_cache,
     return fail(PKV_ERR_INVALID_ARG, "sinks must be contiguous");
   if (lse && (lse->shape[0] != B || lse->shape[1] != Hq))
     return fail(PKV_ERR_INVALID_ARG, "lse must be [B, Hq]");
-  if (block_table->shape[1] < 1 || block_table->shape[1] > (int64_t(1) << 30))
-    return fail(PKV_ERR_INVALID_ARG, "block_table width %lld", (long long)block_table->shape[1]);
+  if ((rc = check_table_width(block_table, page_size))) return rc;
   if (block_table->stride[1] != 1 && block_table->shape[1] > 1)
     return fail(PKV_ERR_INVALID_ARG, "block_table rows must be contiguous");
   if (seq_lens->stride[0] != 1 && B > 1)
@@ -970,6 +988,7 @@ int prepare_gqa_call(const pkv_tensor* q, const pkv_tensor* kv_cache,
   if (num_kv_splits < 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_splits < 0");
   if (B > kGqaMaxBatch)
     return fail(PKV_ERR_UNSUPPORTED, "batch %lld > %d", (long long)B, kGqaMaxBatch);
+  // layout rules of the HND page cache and 16-byte vector access
   if (q->stride[2] != 1 || out->stride[2] != 1 || kv_cache->stride[3] != 1 ||
       kv_cache->stride[2] != 2 * D)
     return fail(PKV_ERR_INVALID_ARG, "q/out last dim and kv_cache rows must be contiguous");
@@ -978,12 +997,17 @@ int prepare_gqa_call(const pkv_tensor* q, const pkv_tensor* kv_cache,
     return fail(PKV_ERR_ALIGNMENT, "strides of q, out and kv_cache must be multiples of 8");
   if (!aligned16(q->data) || !aligned16(out->data) || !aligned16(kv_cache->data))
     return fail(PKV_ERR_ALIGNMENT, "q, out and kv_cache must be 16-byte aligned");
+  if ((rc = check_no_overlap({{out, "out"}, {lse, "lse"}},
+                             {{q, "q"}, {kv_cache, "kv_cache"}, {block_table, "block_table"},
+                              {seq_lens, "seq_lens"}, {sinks, "sinks"}})))
+    return rc;
 
   std::memset(call, 0, sizeof *call);
   call->pairs = B * Hkv;
   call->cap_req = num_kv_splits;
   call->page_size = page_size;
   if (B == 0) return PKV_OK;
+  if ((rc = device_of(q, "q", stream, &call->device))) return rc;
 
   EncodeTiledFn encode = nullptr;
   if ((rc = get_encoder(&encode))) return rc;
@@ -1009,7 +1033,34 @@ int prepare_gqa_call(const pkv_tensor* q, const pkv_tensor* kv_cache,
   p.window = window;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.scale = scale;
-  p.min_pages = 256 / page_size;
+  p.min_pages = 256 / page_size;  // a split streams at least 256 tokens (128 KB per kv head)
+  return PKV_OK;
+}
+
+int gqa_launch_shape(int64_t pairs, int cap_req, int64_t max_items, int64_t max_pairs,
+                     int num_sms, GqaShape* shape) {
+  if (pairs > max_pairs)
+    return fail(PKV_ERR_WORKSPACE, "%lld (request, kv head) pairs exceed the %lld counters",
+                (long long)pairs, (long long)max_pairs);
+  // At most 256 splits per (request, kv head): the merge runs in at most two
+  // levels of at most 16 partials each.
+  int64_t cap = cap_req == 0 ? max_items / pairs : cap_req;
+  if (cap > 256) cap = 256;
+  if (cap < 1) cap = 1;
+  // A launch whose requests cannot split writes no partials and no counters.
+  if (cap > 1 && pairs * cap > max_items)
+    return fail(PKV_ERR_WORKSPACE, "scratch holds %lld split partials, %lld x %lld needed",
+                (long long)max_items, (long long)pairs, (long long)cap);
+  const int64_t grid = std::max<int64_t>(
+      1, std::min<int64_t>(int64_t(num_sms) * gqa_ctas_per_sm(), pairs * cap));
+  shape->cap = int(cap);
+  shape->grid = int(grid);
+  // About four items per CTA (A/B on the Flint batch: best of 2..24), but no
+  // more than 16 per (request, kv head) while that still gives every CTA one:
+  // a few long requests then stream fewer, larger splits, each merged in a
+  // single 16-way level (one 131072-token request, auto cap, on GB300:
+  // 118.7 -> 106.5 us; eight of them 632.8 -> 627.4 us).
+  shape->target_items = int(std::max<int64_t>(grid, std::min<int64_t>(grid * 4, pairs * 16)));
   return PKV_OK;
 }
 

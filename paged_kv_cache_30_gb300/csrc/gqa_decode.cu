@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     if (tid == 0) prefix[B] = total_items;
   }
-  if ((long long)total_items > p.max_items) {
+  if (!one_split && (long long)total_items > p.max_items) {  // one-split items write no partials
     if (tid == 0) atomicOr(p.err, DEVERR_ITEM_OVERFLOW);
     total_items = (int)p.max_items;
   }
@@ -456,7 +456,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     float acc[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-    float m = -INFINITY, l = 0.f;
+    // m: running max (raw logits); msc: the exponent reference m * c2 as
+    // rounded once when m last grew -- every term and rescale uses it, and the
+    // rescale factor is exactly 1 while m holds (a factor recomputed from the
+    // unrounded m * c2 would be 2^(rounding error) != 1 and would compound over
+    // the 8192 tiles of a 131072-key split).  l is a compensated (Neumaier)
+    // sum; lcomp carries the rounding error of its additions.
+    float m = -INFINITY, msc = 0.f, l = 0.f, lcomp = 0.f;
 
     const int ntiles = (d.p1 - d.p0) * TPP;
     for (int k = warp; k < ntiles; k += kConsumerWarps) {
@@ -513,13 +519,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float mn = fmaxf(m, mx);
-      const float msc = (mn == -INFINITY) ? 0.f : mn * c2;
-      const float alpha = ex2(__fmaf_rn(m, c2, -msc));
+      const bool grew = mn > m;  // false while no key has been seen
+      const float msc_new = grew ? mn * c2 : msc;
+      const float alpha = grew ? ((m == -INFINITY) ? 0.f : ex2(msc - msc_new)) : 1.f;
+      msc = msc_new;
       const float e0 = ex2(__fmaf_rn(x0, c2, -msc));
       const float e1 = ex2(__fmaf_rn(x1, c2, -msc));
       const float e2 = ex2(__fmaf_rn(x2, c2, -msc));
       const float e3 = ex2(__fmaf_rn(x3, c2, -msc));
-      l = __fmaf_rn(l, alpha, (e0 + e1) + (e2 + e3));
+      {
+        const float ls = __fmul_rn(l, alpha), x = (e0 + e1) + (e2 + e3);
+        const float tsum = __fadd_rn(ls, x);
+        const bool lbig = fabsf(ls) >= fabsf(x);
+        const float err = __fadd_rn(__fsub_rn(lbig ? ls : x, tsum), lbig ? x : ls);
+        lcomp = __fadd_rn(__fmul_rn(lcomp, alpha), err);
+        l = tsum;
+      }
       m = mn;
       // O^T columns are heads 2t, 2t+1: their rescale factors live on lanes 8t, 8t+4
       const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
@@ -546,6 +561,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 
     // ---- merge the warps' (O, m, l) in shared memory ----
+    l = __fadd_rn(l, lcomp);
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
 #pragma unroll

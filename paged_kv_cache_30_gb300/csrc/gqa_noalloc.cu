@@ -3,9 +3,8 @@
 //
 // Some callers cannot let a library call cudaMalloc: an inference server that
 // hands all of HBM to its own KV-cache pool up front and treats any other
-// device allocation as an out-of-memory risk, a host framework whose memory
-// manager must own every device buffer, or code that has to run while a
-// stream capture forbids allocation.  pkv_paged_decode_attn allocates its
+// device allocation as an out-of-memory risk, or a host framework whose memory
+// manager must own every device buffer.  pkv_paged_decode_attn allocates its
 // workspace on first use; this entry point instead keeps the kernel's scratch
 // (split partials, arrival counters, work-queue words) in one file-scope
 // __device__ array of fixed size, which the CUDA module holds on every device
@@ -42,39 +41,38 @@ DeviceScratch g_dev[64];
 
 }  // namespace
 
+namespace pkv {
+
+// The device error word of the static scratch on `device`, or null when no
+// call has set that device up yet (read by pkv_check_errors).
+int* noalloc_error_word(int device) {
+  if (device < 0 || device >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_dev[device].ready ? reinterpret_cast<int*>(g_dev[device].ptr) + 32 : nullptr;
+}
+
+}  // namespace pkv
+
 extern "C" PKV_API int pkv_paged_decode_attn_noalloc(
     const pkv_tensor* q, const pkv_tensor* kv_cache, const pkv_tensor* block_table,
     const pkv_tensor* seq_lens, const pkv_tensor* sinks, int window, float scale, int page_size,
     int num_kv_splits, const pkv_tensor* out, const pkv_tensor* lse, void* stream_ptr) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   pkv::GqaCall call;
   int rc = pkv::prepare_gqa_call(q, kv_cache, block_table, seq_lens, sinks, window, scale,
-                                 page_size, num_kv_splits, out, lse, &call);
-  if (rc != PKV_OK) return rc;
-  if (call.pairs == 0) return PKV_OK;
-  if (call.pairs > kMaxPairs)
-    return pkv::abi_fail(PKV_ERR_WORKSPACE,
-                         "pkv_paged_decode_attn_noalloc: batch x kv heads exceeds the static "
-                         "scratch limit of 4096 pairs");
-  int64_t cap = call.cap_req == 0 ? kMaxItems / call.pairs : call.cap_req;
-  if (cap > 256) cap = 256;
-  if (cap < 1) cap = 1;
-  if (call.pairs * cap > kMaxItems)
-    return pkv::abi_fail(PKV_ERR_WORKSPACE,
-                         "pkv_paged_decode_attn_noalloc: batch x kv heads x num_kv_splits "
-                         "exceeds the static scratch limit of 2048 split partials");
+                                 page_size, num_kv_splits, out, lse, stream, &call);
+  if (rc != PKV_OK || call.pairs == 0) return rc;
 
-  // Set-up, once per device with that device current: the device address of
-  // the scratch array (in host code its name is only a host-side stand-in).
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return pkv::abi_cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return pkv::abi_fail(PKV_ERR_UNSUPPORTED, "device index above 63");
+  // Set-up, once per device with that device current (prepare_gqa_call has
+  // checked that q's device is current): the device address of the scratch
+  // array (in host code its name is only a host-side stand-in) and the SM count.
+  const int dev = call.device;
   DeviceScratch st;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_dev[dev].ready) {
       void* ptr = nullptr;
-      e = cudaGetSymbolAddress(&ptr, g_scratch);
+      cudaError_t e = cudaGetSymbolAddress(&ptr, g_scratch);
       if (e != cudaSuccess) return pkv::abi_cuda_fail(e, "cudaGetSymbolAddress(scratch)");
       int sms = 0;
       e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -85,28 +83,29 @@ extern "C" PKV_API int pkv_paged_decode_attn_noalloc(
     }
     st = g_dev[dev];
   }
+  // The same launch shape as pkv_paged_decode_attn, on the array's limits.
+  pkv::GqaShape shape;
+  if ((rc = pkv::gqa_launch_shape(call.pairs, call.cap_req, kMaxItems, kMaxPairs, st.num_sms,
+                                  &shape)))
+    return rc;
 
   pkv::GqaParams& p = call.p;
   int* words = reinterpret_cast<int*>(st.ptr);
   p.sched = words;                      // [0] queue head
-  p.err = words + 32;                   // device error bits (not reported on this path)
+  p.err = words + 32;                   // device error bits (pkv_check_errors reads them)
   p.counters = words + 64;              // [kMaxPairs]
   p.group_counters = words + 64 + kMaxPairs;  // [kMaxItems]
   p.part_o = reinterpret_cast<float*>(st.ptr + kCounterInts * 4);
   p.part_ml = p.part_o + kMaxItems * pkv::kGqaPartialFloats;
   p.max_items = kMaxItems;
-  p.cap = int(cap);
-  const int64_t grid64 =
-      std::min<int64_t>(int64_t(st.num_sms) * pkv::gqa_ctas_per_sm(), call.pairs * cap);
-  const int grid = int(grid64 < 1 ? 1 : grid64);
-  p.target_items = grid * 4;  // about four items per CTA (A/B on GB300: best of 2..24)
+  p.cap = shape.cap;
+  p.target_items = shape.target_items;
 
-  // The array keeps the previous call's contents: the queue words and every
-  // arrival counter must start this call at zero.
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  e = cudaMemsetAsync(st.ptr, 0, size_t(kCounterInts) * 4, stream);
+  // The array keeps the previous call's contents: the queue words, the error
+  // word and every arrival counter must start this call at zero.
+  cudaError_t e = cudaMemsetAsync(st.ptr, 0, size_t(kCounterInts) * 4, stream);
   if (e != cudaSuccess) return pkv::abi_cuda_fail(e, "clearing the scratch counters");
-  e = pkv::launch_gqa_decode(p, call.map, call.page_size, grid, stream);
+  e = pkv::launch_gqa_decode(p, call.map, call.page_size, shape.grid, stream);
   if (e != cudaSuccess) return pkv::abi_cuda_fail(e, "gqa decode launch (no-alloc)");
   return PKV_OK;
 }

@@ -83,14 +83,33 @@ struct GqaCall {
   int64_t pairs;   // B * Hkv
   int cap_req;     // num_kv_splits as given (0 = library's choice)
   int page_size;
+  int device;      // the device holding q (current, and the stream's device)
 };
 
 // Defined in api.cpp, for entry points implemented in other files.
+// Validates every argument (shapes, dtypes, strides, alignment, overlap of
+// outputs with inputs, the device of q against the current device and the
+// stream's) and fills `call`; B == 0 returns PKV_OK with call->pairs == 0
+// before any CUDA call.
 int prepare_gqa_call(const ::pkv_tensor* q, const ::pkv_tensor* kv_cache,
                      const ::pkv_tensor* block_table, const ::pkv_tensor* seq_lens,
                      const ::pkv_tensor* sinks, int window, float scale, int page_size,
                      int num_kv_splits, const ::pkv_tensor* out, const ::pkv_tensor* lse,
-                     GqaCall* call);
+                     cudaStream_t stream, GqaCall* call);
+
+// Launch shape of a GQA decode call on scratch that holds max_items split
+// partials and max_pairs (request, kv head) counters: the split cap (0 = the
+// most that fit, at most 256), the grid (CTAs per SM x SMs, or fewer for
+// small calls) and the kernel's target item count.  PKV_ERR_WORKSPACE when
+// the call does not fit.  Every entry point launching the GQA kernel uses it.
+struct GqaShape {
+  int cap, grid, target_items;
+};
+int gqa_launch_shape(int64_t pairs, int cap_req, int64_t max_items, int64_t max_pairs,
+                     int num_sms, GqaShape* shape);
+// Device address of the error word of pkv_paged_decode_attn_noalloc's static
+// scratch on `device`, or null before that device's first such call.
+int* noalloc_error_word(int device);
 int abi_fail(int code, const char* message);
 int abi_cuda_fail(cudaError_t e, const char* what);
 

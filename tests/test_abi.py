@@ -58,11 +58,19 @@ def _t(shape, dtype, strides=None, ptr=0x10000):
     return d
 
 
+# Fake device addresses, far enough apart that no two default views overlap
+# (validation happens before any CUDA call, so nothing is dereferenced).
+PTR = dict(q=0x1000000, kv=0x2000000, bt=0x8000000, sl=0x9000000, out=0xa000000,
+           lse=0xb000000, sinks=0xc000000)
+
+
 def _gqa_args(B=2, Hq=16, Hkv=2, D=128, P=16, nb=64, maxb=8):
     return dict(
-        q=_t([B, Hq, D], pkv.DTYPE_BF16), kv=_t([nb, Hkv, P, 2 * D], pkv.DTYPE_BF16),
-        bt=_t([B, maxb], pkv.DTYPE_I32), sl=_t([B], pkv.DTYPE_I32),
-        out=_t([B, Hq, D], pkv.DTYPE_BF16, ptr=0x20000), lse=_t([B, Hq], pkv.DTYPE_F32))
+        q=_t([B, Hq, D], pkv.DTYPE_BF16, ptr=PTR["q"]),
+        kv=_t([nb, Hkv, P, 2 * D], pkv.DTYPE_BF16, ptr=PTR["kv"]),
+        bt=_t([B, maxb], pkv.DTYPE_I32, ptr=PTR["bt"]), sl=_t([B], pkv.DTYPE_I32, ptr=PTR["sl"]),
+        out=_t([B, Hq, D], pkv.DTYPE_BF16, ptr=PTR["out"]),
+        lse=_t([B, Hq], pkv.DTYPE_F32, ptr=PTR["lse"]))
 
 
 def _call(lib, a, sinks=None, window=0, scale=0.088, P=16, cap=0):
@@ -78,13 +86,23 @@ def _call(lib, a, sinks=None, window=0, scale=0.088, P=16, cap=0):
     (lambda a: a.update(kv=_t([64, 2, 8, 256], pkv.DTYPE_BF16)), -1),          # P mismatch
     (lambda a: a.update(q=_t([2, 16, 128], pkv.DTYPE_F32)), -1),               # dtype
     (lambda a: a.update(bt=_t([3, 8], pkv.DTYPE_I32)), -1),                    # batch mismatch
-    (lambda a: a.update(q=_t([2, 16, 128], pkv.DTYPE_BF16, ptr=0x10008)), -3),  # alignment
-    (lambda a: a.update(kv=_t([64, 2, 16, 256], pkv.DTYPE_BF16, [8196, 4098, 256, 1])), -3),
-    (lambda a: a.update(kv=_t([64, 2, 16, 256], pkv.DTYPE_BF16, [8192, 4096, 512, 1])), -1),
+    (lambda a: a.update(q=_t([2, 16, 128], pkv.DTYPE_BF16, ptr=PTR["q"] + 8)), -3),  # alignment
+    (lambda a: a.update(kv=_t([64, 2, 16, 256], pkv.DTYPE_BF16, [8196, 4098, 256, 1],
+                              ptr=PTR["kv"])), -3),
+    (lambda a: a.update(kv=_t([64, 2, 16, 256], pkv.DTYPE_BF16, [8192, 4096, 512, 1],
+                              ptr=PTR["kv"])), -1),
     (lambda a: a.update(q=_t([4096, 16, 128], pkv.DTYPE_BF16),
                         bt=_t([4096, 8], pkv.DTYPE_I32), sl=_t([4096], pkv.DTYPE_I32),
                         out=_t([4096, 16, 128], pkv.DTYPE_BF16),
                         lse=_t([4096, 16], pkv.DTYPE_F32)), -2),               # batch > 2048
+    # outputs sharing memory with an input or with each other
+    (lambda a: a.update(out=_t([2, 16, 128], pkv.DTYPE_BF16, ptr=PTR["q"])), -1),
+    (lambda a: a.update(out=_t([2, 16, 128], pkv.DTYPE_BF16, ptr=PTR["q"] + 4096)), -1),
+    (lambda a: a.update(lse=_t([2, 16], pkv.DTYPE_F32, ptr=PTR["out"] + 64)), -1),
+    (lambda a: a.update(lse=_t([2, 16], pkv.DTYPE_F32, ptr=PTR["kv"] + 1024)), -1),
+    (lambda a: a.update(out=_t([2, 16, 128], pkv.DTYPE_BF16, ptr=PTR["bt"])), -1),
+    # block-table width x page size must stay below 2^31
+    (lambda a: a.update(bt=_t([2, 1 << 27], pkv.DTYPE_I32, ptr=PTR["bt"])), -1),
 ])
 def test_gqa_validation_rejects_before_any_cuda_call(lib, mutate, code):
     a = _gqa_args()
@@ -103,6 +121,16 @@ def test_gqa_validation_page_size_and_args(lib):
     r = ctypes.byref
     assert lib.pkv_paged_decode_attn(None, r(a["kv"]), r(a["bt"]), r(a["sl"]), None, 0, 1.0,
                                      16, 0, r(a["out"]), None, None) == -1
+
+
+def test_gqa_outputs_adjacent_to_inputs_are_accepted_by_validation(lib):
+    """out ending exactly where q begins is not an overlap: validation passes,
+    and the call fails only later, at the first CUDA call (no GPU here)."""
+    a = _gqa_args()
+    q_bytes = 2 * 16 * 128 * 2
+    a["out"] = _t([2, 16, 128], pkv.DTYPE_BF16, ptr=PTR["q"] - q_bytes)
+    rc = _call(lib, a)
+    assert rc != -1 or "overlaps" not in pkv.last_error()
 
 
 def test_gqa_empty_batch_is_a_no_op(lib):
@@ -246,3 +274,47 @@ def test_quantize_validation_rejects_before_any_cuda_call(lib, mutate, code):
     r = ctypes.byref
     assert lib.pkv_mla_quantize_q(r(a["q"]), r(a["q8"]), r(a["qs"]), None) == code
     assert pkv.last_error()
+
+
+# ------------------------------------------- overlapping outputs, any path --
+def test_mla_outputs_overlapping_inputs_are_rejected(lib):
+    def args():
+        return dict(q8=_t([4, 128, 576], pkv.DTYPE_FP8, ptr=PTR["q"]),
+                    qs=_t([4, 128], pkv.DTYPE_F32, ptr=PTR["sinks"]),
+                    c=_t([64, 16, 1, 576], pkv.DTYPE_FP8, ptr=PTR["kv"]),
+                    bt=_t([4, 8], pkv.DTYPE_I32, ptr=PTR["bt"]),
+                    sl=_t([4], pkv.DTYPE_I32, ptr=PTR["sl"]),
+                    out=_t([4, 128, 512], pkv.DTYPE_BF16, ptr=PTR["out"]),
+                    lse=_t([4, 128], pkv.DTYPE_F32, ptr=PTR["lse"]))
+    for name, ptr in (("out", PTR["q"] + 4096), ("out", PTR["kv"]), ("lse", PTR["out"] + 512),
+                      ("lse", PTR["sinks"])):
+        a = args()
+        t = a[name]
+        a[name] = _t([t.shape[i] for i in range(t.ndim)], t.dtype, ptr=ptr)
+        assert _nat_call(lib, a) == -1, name
+        assert "overlaps" in pkv.last_error()
+
+
+def test_append_and_quantize_outputs_overlapping_inputs_are_rejected(lib):
+    a = dict(k=_t([2, 2, 128], pkv.DTYPE_BF16, ptr=PTR["q"]),
+             v=_t([2, 2, 128], pkv.DTYPE_BF16, ptr=PTR["out"]),
+             kv=_t([64, 2, 16, 256], pkv.DTYPE_BF16, ptr=PTR["kv"]),
+             bt=_t([2, 8], pkv.DTYPE_I32, ptr=PTR["bt"]), sl=_t([2], pkv.DTYPE_I32, ptr=PTR["sl"]))
+    a["v"] = _t([2, 2, 128], pkv.DTYPE_BF16, ptr=PTR["kv"] + 8192)  # v inside the cache
+    assert _append(lib, a) == -1 and "overlaps" in pkv.last_error()
+    r = ctypes.byref
+    q = _t([4, 128, 576], pkv.DTYPE_BF16, ptr=PTR["q"])
+    q8 = _t([4, 128, 576], pkv.DTYPE_FP8, ptr=PTR["q"] + 65536)  # inside q
+    qs = _t([4, 128], pkv.DTYPE_F32, ptr=PTR["lse"])
+    assert lib.pkv_mla_quantize_q(r(q), r(q8), r(qs), None) == -1
+    assert "overlaps" in pkv.last_error()
+
+
+def test_block_table_width_times_page_size_must_fit_31_bits(lib):
+    r = ctypes.byref
+    lat = _t([8, 576], pkv.DTYPE_BF16, ptr=PTR["q"])
+    cache = _t([32, 16, 1, 576], pkv.DTYPE_BF16, ptr=PTR["kv"])
+    sl = _t([4], pkv.DTYPE_I32, ptr=PTR["sl"])
+    wide = _t([4, 1 << 27], pkv.DTYPE_I32, ptr=PTR["bt"])  # 2^27 x 16 = 2^31
+    assert lib.pkv_mla_kv_append(r(lat), r(cache), r(wide), r(sl), 2, 16, None, None) == -1
+    assert "2^31" in pkv.last_error()

@@ -17,9 +17,10 @@ pytestmark = pytest.mark.gpu
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 # Between two split counts of the same call: bf16 outputs within 2e-3, lse
-# within 3e-4 (fp32 accumulation order only; each is also within the oracle
-# tolerance of 1e-3 on its own).
-LSE_INVARIANCE = 3e-4
+# within 1e-4 (fp32 accumulation order only; each lane's running sum of the
+# softmax denominator is compensated, so a single split of 131072 keys stays
+# as accurate as many short ones).
+LSE_INVARIANCE = 1e-4
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -339,3 +340,22 @@ def test_long_context_split_sweep_every_row(B):
         assert np.max(np.abs(lse - l1)) <= LSE_INVARIANCE, f"B={B} cap {cap}: lse vs cap 1"
     del d
     torch.cuda.empty_cache()
+
+
+def test_inputs_outside_device_memory_are_rejected_before_launch():
+    """The call's device is the device holding q: a q in host memory (pinned or
+    pageable) is refused with PKV_ERR_INVALID_ARG and nothing is written."""
+    import ctypes
+    prob = W.tiny_gqa(0)
+    d = dict(kv=dev(prob.kv_cache), bt=dev(prob.block_table), sl=dev(prob.seq_lens))
+    out = torch.full((4, 8, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lib = pkv.load_library()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    D = pkv._desc
+    for q in (prob.q.clone(), prob.q.pin_memory()):
+        for entry in ("pkv_paged_decode_attn", "pkv_paged_decode_attn_noalloc"):
+            rc = getattr(lib, entry)(D(q), D(d["kv"]), D(d["bt"]), D(d["sl"]), None, 0,
+                                     float(prob.scale), 16, 4, D(out), None, stream)
+            assert rc == -1 and "not device memory" in pkv.last_error(), entry
+    torch.cuda.synchronize()
+    assert torch.isnan(out.float()).all()

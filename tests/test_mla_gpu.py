@@ -112,22 +112,23 @@ def test_mla_degenerate_warmup_inputs():
 
 # Between two split counts of one MLA call.  Measured on GB300 (this test's
 # problem and the B=32 qlen-4 workload, caps 1, 2, 5, 8, 16 against cap 1):
-# outputs differ by at most one bf16 ulp of the output (7.8e-3 at |out| = 1.08,
-# where an ulp is 2^-7; 99th percentile 4.9e-4) and lse by 9.5e-7.  The fp32
-# results of two split counts differ only by accumulation order (~1e-6
-# relative) and each is rounded once to bf16, so where they straddle a rounding
-# boundary they land one ulp apart: the bound is relative to the output's
-# magnitude, not an absolute 2e-3 (GQA outputs stay below ~0.25, where one ulp
-# is at most 2^-10).
+# outputs near zero differ by up to ~2e-4 (99th percentile of all differences
+# 4.9e-4): each split rounds P to bf16 against its own reference max, the same
+# noise the GQA kernel's absolute 2e-3 bound covers; outputs of magnitude ~1
+# (rows with few keys) differ by at most one bf16 ulp (7.8e-3 at |out| = 1.08,
+# where an ulp is 2^-7), because two fp32 results that differ by ~1e-6 round
+# to adjacent bf16 values.  lse differs by at most 9.5e-7.  Bound: every
+# element within max(2e-3, one bf16 ulp of the larger magnitude); lse 1e-5.
 MLA_INV_ULPS = 1.0
+MLA_INV_ABS = 2e-3
 MLA_INV_LSE = 1e-5
 
 
 def check_split_invariance(outs, what):
     o1, l1 = outs[0]
     for i, (out, lse) in enumerate(outs[1:], 1):
-        assert within_bf16_reorder(out, o1, ulps=MLA_INV_ULPS, floor=1e-4), \
-            f"{what} #{i}: out more than {MLA_INV_ULPS} bf16 ulp from cap 1"
+        assert within_bf16_reorder(out, o1, ulps=MLA_INV_ULPS, floor=MLA_INV_ABS), \
+            f"{what} #{i}: out beyond max({MLA_INV_ABS}, {MLA_INV_ULPS} bf16 ulp) from cap 1"
         fin = np.isfinite(l1)
         assert np.array_equal(fin, np.isfinite(lse))
         d_lse = float(np.max(np.abs(lse[fin] - l1[fin]))) if fin.any() else 0.0
