@@ -54,6 +54,18 @@
  *    been made from a live stream, or after pkv_shutdown()).  No event is
  *    recorded between calls on one stream, which keeps consecutive launches
  *    overlapping (programmatic dependent launch).
+ *  - Programmatic dependent launch: the attention kernels launch as dependents
+ *    of the kernel before them on the stream and may start while it runs.
+ *    Before waiting for it, pkv_paged_decode_attn (and its no-alloc variant)
+ *    reads seq_lens, block_table and up to 8 tiles of the leading KV pages of
+ *    each CTA's first work item -- never the page holding position
+ *    seq_len - 1.  So seq_lens, block_table and the cache pages before the
+ *    current token's must not be written by a kernel that may still be running
+ *    when the call's kernel starts (the kernel immediately before it on the
+ *    stream, or one an earlier dependent launch let run early).  Writing the
+ *    current token's slot right before the call (pkv_gqa_kv_append) is fine,
+ *    as is anything written by copies or by kernels that completed.  q, sinks,
+ *    the workspace and all outputs are touched only after the wait.
  *  - The launch shape depends only on the device and the batch size, never on
  *    the sequence lengths or the block table, which the kernels read on the
  *    device: a captured graph stays valid when seq_lens and block_table change.

@@ -13,13 +13,18 @@
 //    same item list in its prologue from seq_lens alone: request b's n_b
 //    attended pages are cut into s_b = min(cap, ceil(n_b / chunk)) contiguous
 //    page ranges, with chunk chosen from the total so that the launch has about
-//    target_items items (shorter requests use fewer splits).  CTAs pull items
-//    from a global queue (an atomic head; every CTA fetches until it draws an
-//    index past the end, so the launch makes exactly items + CTAs fetches and
-//    the CTA that draws the last one resets the head to zero), so the launch
-//    shape depends only on the device and the batch.  A CTA claims its next
-//    item only when the current one has a few tiles left to issue, so when the
-//    queue runs dry no CTA still holds an unstarted item.
+//    target_items items (shorter requests use fewer splits).  CTA c starts
+//    with item c; the rest come from a global queue (an atomic head; every CTA
+//    fetches until it draws an index past the end, so the launch makes a known
+//    number of fetches and the CTA that draws the last one resets the head to
+//    zero), so the launch shape depends only on the device and the batch.  A
+//    CTA claims its next item only when the current one has a few tiles left
+//    to issue, so when the queue runs dry no CTA still holds an unstarted item.
+//  * Programmatic dependent launch: the prologue, the first item's descriptor,
+//    its block-table entries and up to one ring of its leading tiles (never
+//    the page holding position L - 1) are done before griddepcontrol.wait, so
+//    they overlap the tail of the kernel before; q, the queue, the workspace
+//    and the outputs come after it.
 //  * The first producer warp takes items from the queue, writes each item's
 //    descriptor and bulk-copies its 8 query rows into a descriptor slot.  Both
 //    producer warps read block-table entries 32 at a time and stream the
@@ -69,7 +74,9 @@ constexpr int kClaimTiles = 4;         // claim the next item this many tiles be
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct ItemDesc {
-  int item, b, kvh, split, nsplit, p0, p1, start_tok, L, seq_base, pad0, pad1;
+  // pe: pages [p0, pe) of a CTA's first item are streamed before the
+  // programmatic-dependent-launch wait (pe == p0 for later items)
+  int item, b, kvh, split, nsplit, p0, p1, start_tok, L, seq_base, pe, pad1;
 };
 
 // shared-memory carve-up (offsets from a 1024-aligned base)
@@ -230,13 +237,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     fence_barrier_init();
   }
   if (warp == kConsumerWarps && lane == 0) tma_prefetch_desc(&kv_map);
-  // Programmatic dependent launch: the setup above touches only shared memory
-  // and the kernel parameters; the inputs and the workspace are read after the
-  // grids this launch depends on (e.g. the previous call) have completed.
-  griddep_wait();
-  // The first queue fetch is issued now: its latency overlaps the prologue.
-  int first_item = 0;
-  if (warp == kConsumerWarps && lane == 0) first_item = atomicAdd(&p.sched[0], 1);
+  // Programmatic dependent launch.  Before griddepcontrol.wait (i.e. while the
+  // grid this launch depends on, e.g. the previous call or layer, may still be
+  // running) the kernel reads only seq_lens, block_table and the leading KV
+  // pages of its first item -- never the page holding position L - 1, which
+  // an append kernel may just have written -- and writes only shared memory
+  // (and error bits).  q, sinks, the workspace (queue, counters, partials)
+  // and every output are touched after the wait.
 
   // ---- prologue: the item list, identical in every CTA -------------------
   const int B = p.B;
@@ -327,7 +334,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       __syncwarp();
       if (lane == 0) mbar_arrive(iempty_bar(slot));
       if (d.item < 0) break;
-      stream_tiles(p.bt + (long long)d.b * p.bt_sb, d.kvh, d.p0, d.p1, (uint32_t)d.seq_base, 1u,
+      const int32_t* bt_row = p.bt + (long long)d.b * p.bt_sb;
+      stream_tiles(bt_row, d.kvh, d.p0, d.pe, (uint32_t)d.seq_base, 1u, -1, [] {});
+      if (it == 0) griddep_wait();  // the pages from pe on only after the wait
+      stream_tiles(bt_row, d.kvh, d.pe, d.p1, (uint32_t)(d.seq_base + (d.pe - d.p0) * TPP), 1u,
                    -1, [] {});
     }
     return;
@@ -335,24 +345,40 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   if (warp == kConsumerWarps) {
     // ============ first producer warp: the queue, descriptors, even tiles ============
-    // The fetch that returns total_items + gridDim.x - 1 is the launch's last
-    // (each CTA stops after its first index past the end): it resets the head.
-    // The next item is claimed only when the current one has kClaimTiles
-    // tiles left to issue (enough to hide the atomic): a claimed item waits
-    // for the current one to end, so claiming at its start would leave a CTA
-    // holding up to two items when the queue runs dry.
-    const int last_fetch = total_items + (int)gridDim.x - 1;
-    int fetched = first_item;  // lane 0's claim, not yet examined
+    // CTA c's first item is item c (static: known before the wait, so its
+    // leading tiles are requested then); the queue deals items gridDim.x on.
+    // A CTA claims its next item when the current one has kClaimTiles tiles
+    // left to issue (enough to hide the atomic): a claimed item waits for the
+    // current one to end, so claiming at its start would leave a CTA holding
+    // up to two items when the queue runs dry.  Every CTA draws exactly one
+    // queue index past the end, so the launch makes (items beyond the static
+    // ones) + CTAs fetches, and the fetch that returns the last of them resets
+    // the head.
+    const int grid = (int)gridDim.x;
+    const int last_fetch = max(total_items - grid, 0) + grid - 1;
+    int fetched = 0;  // lane 0's claim (a queue index), not yet examined
     uint32_t seq = 0;
     for (int it = 0;; ++it) {
-      const int item = __shfl_sync(0xffffffffu, fetched, 0);
-      if (lane == 0 && item == last_fetch) atomicExch(&p.sched[0], 0);
+      int item = (int)blockIdx.x;
+      if (it > 0) {
+        const int k = __shfl_sync(0xffffffffu, fetched, 0);
+        if (lane == 0 && k == last_fetch) atomicExch(&p.sched[0], 0);
+        item = grid + k;
+      }
       const int slot = it % kItemSlots;
       if (lane == 0) mbar_wait(iempty_bar(slot), ((it / kItemSlots) & 1) ^ 1u, p.err);
       __syncwarp();
       // no CTA can take more items than the launch has: the item loop is bounded
       const bool runaway = it > total_items;
       if (item >= total_items || runaway) {
+        if (it == 0) {
+          // no static item: this CTA still draws its one index past the end
+          griddep_wait();
+          if (lane == 0) {
+            const int k = atomicAdd(&p.sched[0], 1);
+            if (k == last_fetch) atomicExch(&p.sched[0], 0);
+          }
+        }
         if (lane == 0) {
           if (runaway) atomicOr(p.err, DEVERR_QUEUE);
           griddep_launch_dependents();  // the queue is empty: this CTA only drains now
@@ -389,13 +415,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int n = (L + P - 1) / P - sp;
       const int p0 = sp + (int)((long long)n * split / nsplit);
       const int p1 = sp + (int)((long long)n * (split + 1) / nsplit);
+      // First item: pages before the one holding position L - 1, at most one
+      // ring's worth (both producers together issue at most kStages tiles, so
+      // neither waits for a free stage before the consumers can start).
+      const int pe = it == 0 ? max(p0, min(min(p1, p0 + kStages / TPP), (L - 1) / P)) : p0;
       if (lane == 0) {
         ItemDesc& d = items[slot];
         d.item = item; d.b = b; d.kvh = kvh; d.split = split; d.nsplit = nsplit;
         d.p0 = p0; d.p1 = p1; d.start_tok = start_tok; d.L = L; d.seq_base = (int)seq;
-        // the descriptor stores are released by these arrives; the consumers'
-        // phase also waits for the 8 query rows
+        d.pe = pe;
+        // the descriptor stores are released by this arrive
         mbar_arrive(dfull_bar(slot));
+      }
+      const int32_t* bt_row = p.bt + (long long)b * p.bt_sb;
+      stream_tiles(bt_row, kvh, p0, pe, seq, 0u, -1, [] {});
+      if (it == 0) griddep_wait();
+      if (lane == 0) {
+        // the consumers' phase also waits for the 8 query rows
         mbar_arrive_expect_tx(ifull_bar(slot), kQBytes);
         const uint16_t* qrow = p.q + b * p.q_sb + (long long)(kvh * kGqaGroup) * p.q_sh;
 #pragma unroll
@@ -403,12 +439,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           bulk_load(qbuf + slot * kQBytes + h * kGqaHeadDim * 2, qrow + h * p.q_sh,
                     kGqaHeadDim * 2, ifull_bar(slot));
       }
-      // claim_at lies in [p0, p1) for any item with pages, so every item claims once
-      const int claim_at = max(p0, p1 - max(1, kClaimTiles / TPP));
-      stream_tiles(p.bt + (long long)b * p.bt_sb, kvh, p0, p1, seq, 0u, claim_at, [&] {
+      // claim_at lies in [pe, p1) whenever pages remain after pe; otherwise the
+      // claim is made right away
+      const int claim_at = max(pe, p1 - max(1, kClaimTiles / TPP));
+      stream_tiles(bt_row, kvh, pe, p1, seq + (uint32_t)((pe - p0) * TPP), 0u, claim_at, [&] {
         if (lane == 0) fetched = atomicAdd(&p.sched[0], 1);
       });
-      if (p1 <= p0 && lane == 0) fetched = atomicAdd(&p.sched[0], 1);  // an item of no pages
+      if (p1 <= pe && lane == 0) fetched = atomicAdd(&p.sched[0], 1);
       seq += (uint32_t)((p1 - p0) * TPP);
     }
     if (lane == 0) {
@@ -422,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
 
   // ============================ consumer warps ============================
+  griddep_wait();  // outputs, partials and counters only after the wait
   const int g = lane >> 2, t = lane & 3;
   // ldmatrix addressing: matrix mi = lane / 8 supplies row r = lane % 8 of
   // tile rows 0..7 (mi = 0, 1) or 8..15 (mi = 2, 3); odd mi read the upper

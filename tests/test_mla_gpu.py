@@ -7,7 +7,7 @@ import torch
 import oracle
 import paged_kv_cache_30_gb300 as pkv
 from paged_kv_cache_30_gb300 import workloads as W
-from tests.gpu_helpers import TOL_LSE, TOL_OUT, TOL_OUT_FP8, compare, within_bf16_reorder
+from tests.gpu_helpers import TOL_LSE, TOL_OUT, TOL_OUT_FP8, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -112,23 +112,28 @@ def test_mla_degenerate_warmup_inputs():
 
 # Between two split counts of one MLA call.  Measured on GB300 (this test's
 # problem and the B=32 qlen-4 workload, caps 1, 2, 5, 8, 16 against cap 1):
-# outputs near zero differ by up to ~2e-4 (99th percentile of all differences
-# 4.9e-4): each split rounds P to bf16 against its own reference max, the same
-# noise the GQA kernel's absolute 2e-3 bound covers; outputs of magnitude ~1
-# (rows with few keys) differ by at most one bf16 ulp (7.8e-3 at |out| = 1.08,
-# where an ulp is 2^-7), because two fp32 results that differ by ~1e-6 round
-# to adjacent bf16 values.  lse differs by at most 9.5e-7.  Bound: every
-# element within max(2e-3, one bf16 ulp of the larger magnitude); lse 1e-5.
-MLA_INV_ULPS = 1.0
+# outputs below 0.25 in magnitude differ by at most 1.95e-3: each split rounds
+# P to bf16 against its own reference max, the same noise the GQA kernel's
+# absolute 2e-3 bound covers.  Larger outputs (rows with few keys) add the
+# final rounding: two fp32 results that differ by that noise round to bf16
+# values up to one ulp further apart (worst seen: 3.9e-3 at |out| = 0.48,
+# where an ulp is 2^-9, and 7.8e-3 at |out| = 1.08, where it is 2^-7).  lse
+# differs by at most 9.5e-7.  Bound: every element within 2e-3 plus one bf16
+# ulp of the larger magnitude; lse within 1e-5.
 MLA_INV_ABS = 2e-3
 MLA_INV_LSE = 1e-5
 
 
 def check_split_invariance(outs, what):
     o1, l1 = outs[0]
+    o1 = o1.astype(np.float64)
     for i, (out, lse) in enumerate(outs[1:], 1):
-        assert within_bf16_reorder(out, o1, ulps=MLA_INV_ULPS, floor=MLA_INV_ABS), \
-            f"{what} #{i}: out beyond max({MLA_INV_ABS}, {MLA_INV_ULPS} bf16 ulp) from cap 1"
+        out = out.astype(np.float64)
+        mag = np.maximum(np.maximum(np.abs(out), np.abs(o1)), 2.0 ** -100)
+        ulp = 2.0 ** (np.floor(np.log2(mag)) - 7)
+        excess = np.abs(out - o1) - (MLA_INV_ABS + ulp)
+        assert np.all(excess <= 0), \
+            f"{what} #{i}: out beyond 2e-3 + 1 bf16 ulp from cap 1 (by {excess.max():.3g})"
         fin = np.isfinite(l1)
         assert np.array_equal(fin, np.isfinite(lse))
         d_lse = float(np.max(np.abs(lse[fin] - l1[fin]))) if fin.any() else 0.0
