@@ -452,10 +452,11 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
       std::min<int64_t>(int64_t(ws.partial_bytes) / item_bytes, ws.num_counters - pkv::kTopCounters);
   pkv::GqaShape shape;
   if ((rc = pkv::gqa_launch_shape(call.pairs, call.cap_req, max_items, pkv::kTopCounters,
-                                  ws.num_sms, &shape)))
+                                  ws.num_sms, call.p.max_blocks, page_size, &shape)))
     return rc;
   pkv::GqaParams& p = call.p;
-  p.cap = shape.cap;
+  p.cap = shape.cluster > 1 ? shape.cluster : shape.cap;
+  p.cluster = shape.cluster;
   p.target_items = shape.target_items;
   p.part_o = ws.partials;
   p.part_ml = ws.partials + max_items * pkv::kGqaPartialFloats;
@@ -1038,7 +1039,7 @@ int prepare_gqa_call(const pkv_tensor* q, const pkv_tensor* kv_cache,
 }
 
 int gqa_launch_shape(int64_t pairs, int cap_req, int64_t max_items, int64_t max_pairs,
-                     int num_sms, GqaShape* shape) {
+                     int num_sms, int max_blocks, int page_size, GqaShape* shape) {
   if (pairs > max_pairs)
     return fail(PKV_ERR_WORKSPACE, "%lld (request, kv head) pairs exceed the %lld counters",
                 (long long)pairs, (long long)max_pairs);
@@ -1061,6 +1062,18 @@ int gqa_launch_shape(int64_t pairs, int cap_req, int64_t max_items, int64_t max_
   // single 16-way level (one 131072-token request, auto cap, on GB300:
   // 118.7 -> 106.5 us; eight of them 632.8 -> 627.4 us).
   shape->target_items = int(std::max<int64_t>(grid, std::min<int64_t>(grid * 4, pairs * 16)));
+  // Cluster mode (splits merged through distributed shared memory, no queue
+  // and no workspace partials) for small launches whose requests are short:
+  // C = splits a request of the block table's full width can use (at most 8,
+  // at least 256 keys each), when every (request, kv head) gets its own
+  // cluster in a single wave and no split can exceed 64 pages.
+  const int64_t min_pages = 256 / page_size;
+  const int64_t c = std::min<int64_t>(
+      std::min<int64_t>(cap, kGqaMaxCluster), (int64_t(max_blocks) + min_pages - 1) / min_pages);
+  shape->cluster = 0;
+  if (c >= 2 && c * pairs <= int64_t(num_sms) * gqa_ctas_per_sm() &&
+      (int64_t(max_blocks) + c - 1) / c <= 64)
+    shape->cluster = int(c);
   return PKV_OK;
 }
 

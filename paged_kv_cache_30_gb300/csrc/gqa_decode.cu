@@ -198,7 +198,7 @@ __device__ __forceinline__ void store_partial(const GqaParams& p, long long slot
   }
 }
 
-template <int P>
+template <int P, bool kCluster>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     gqa_decode_kernel(const __grid_constant__ GqaParams p,
                       const __grid_constant__ CUtensorMap kv_map) {
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // tokens touches at most (W + 2P - 2) / P pages.
   const bool one_split = p.cap <= 1 || (p.window > 0 && (p.window + 2 * P - 2) / P <= p.min_pages);
   int total_items = B * p.Hkv;
-  if (!one_split) {
+  if (!kCluster && !one_split) {
     int local_pages = 0;
     for (int b = tid; b < B; b += kThreads) {
       const int raw = __ldg(p.seq_lens + b);
@@ -284,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     if (tid == 0) prefix[B] = total_items;
   }
-  if (!one_split && (long long)total_items > p.max_items) {  // one-split items write no partials
+  // one-split items and the cluster mode write no partials
+  if (!kCluster && !one_split && (long long)total_items > p.max_items) {
     if (tid == 0) atomicOr(p.err, DEVERR_ITEM_OVERFLOW);
     total_items = (int)p.max_items;
   }
@@ -325,6 +326,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
   };
 
+  // cluster mode: the split this CTA's consumers left in shared memory
+  int cl_nsplit = 0, cl_b = 0, cl_kvh = 0;
+  const int eh = (tid & (kConsumers - 1)) >> 4, ed = (tid & 15) * 8;  // epilogue: head, 8 dims
+
   if (warp == kConsumerWarps + 1) {
     // ===================== second producer warp: odd tiles =====================
     for (int it = 0;; ++it) {
@@ -340,10 +345,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       stream_tiles(bt_row, d.kvh, d.pe, d.p1, (uint32_t)(d.seq_base + (d.pe - d.p0) * TPP), 1u,
                    -1, [] {});
     }
-    return;
-  }
-
-  if (warp == kConsumerWarps) {
+  } else if (warp == kConsumerWarps) {
     // ============ first producer warp: the queue, descriptors, even tiles ============
     // CTA c's first item is item c (static: known before the wait, so its
     // leading tiles are requested then); the queue deals items gridDim.x on.
@@ -360,7 +362,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint32_t seq = 0;
     for (int it = 0;; ++it) {
       int item = (int)blockIdx.x;
-      if (it > 0) {
+      // cluster mode: one item, split blockIdx.x of (request, kv head) blockIdx.y
+      int b = 0, nsplit = 1, kvh = 0, split = 0, L = 0;
+      if (kCluster) {
+        const int pair = (int)blockIdx.y;
+        b = pair / p.Hkv;
+        kvh = pair - b * p.Hkv;
+        split = (int)blockIdx.x;
+        L = clamp_len<P>(p, b);
+        if (lane == 0 && kvh == 0 && split == 0 &&
+            (long long)__ldg(p.seq_lens + b) > (long long)p.max_blocks * P)
+          atomicOr(p.err, DEVERR_SEQ_TOO_LONG);
+        const int n = (L + P - 1) / P - window_start(p, L) / P;
+        nsplit = max(1, min(p.cluster, (n + p.min_pages - 1) / p.min_pages));
+        item = (it == 0 && split < nsplit) ? pair : total_items;
+      } else if (it > 0) {
         const int k = __shfl_sync(0xffffffffu, fetched, 0);
         if (lane == 0 && k == last_fetch) atomicExch(&p.sched[0], 0);
         item = grid + k;
@@ -371,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // no CTA can take more items than the launch has: the item loop is bounded
       const bool runaway = it > total_items;
       if (item >= total_items || runaway) {
-        if (it == 0) {
+        if (!kCluster && it == 0) {
           // no static item: this CTA still draws its one index past the end
           griddep_wait();
           if (lane == 0) {
@@ -388,8 +404,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         break;
       }
-      int b, nsplit, kvh, split;
-      if (one_split) {
+      if (kCluster) {
+        // (b, kvh, split, nsplit, L) decoded above
+      } else if (one_split) {
         b = item / p.Hkv;
         kvh = item - b * p.Hkv;
         nsplit = 1;
@@ -409,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         kvh = local / nsplit;
         split = local % nsplit;
       }
-      const int L = clamp_len<P>(p, b);
+      if (!kCluster) L = clamp_len<P>(p, b);
       const int start_tok = window_start(p, L);
       const int sp = start_tok / P;
       const int n = (L + P - 1) / P - sp;
@@ -441,11 +458,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       // claim_at lies in [pe, p1) whenever pages remain after pe; otherwise the
       // claim is made right away
-      const int claim_at = max(pe, p1 - max(1, kClaimTiles / TPP));
+      // (the cluster mode has no queue: one item per CTA)
+      const int claim_at = kCluster ? -1 : max(pe, p1 - max(1, kClaimTiles / TPP));
       stream_tiles(bt_row, kvh, pe, p1, seq + (uint32_t)((pe - p0) * TPP), 0u, claim_at, [&] {
         if (lane == 0) fetched = atomicAdd(&p.sched[0], 1);
       });
-      if (p1 <= pe && lane == 0) fetched = atomicAdd(&p.sched[0], 1);
+      if (!kCluster && p1 <= pe && lane == 0) fetched = atomicAdd(&p.sched[0], 1);
       seq += (uint32_t)((p1 - p0) * TPP);
     }
     if (lane == 0) {
@@ -455,9 +473,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       for (uint32_t k = seq - recent; k < seq; ++k)
         mbar_wait(full_bar(k % kStages), (k / kStages) & 1, p.err);
     }
-    return;
-  }
-
+  } else {
   // ============================ consumer warps ============================
   griddep_wait();  // outputs, partials and counters only after the wait
   const int g = lane >> 2, t = lane & 3;
@@ -469,7 +485,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const uint32_t row_off = (uint32_t)(r + 8 * (mi >> 1)) * 128u;
   const int ubit = mi & 1;
   float* my_wb = wbuf + warp * kWbFloats;
-  const int eh = tid >> 4, ed = (tid & 15) * 8;  // epilogue: head, first of 8 dims
   const float c2 = p.scale_log2;
 
   for (int it = 0;; ++it) {
@@ -638,6 +653,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int head = d.kvh * kGqaGroup + eh;
     if (d.nsplit == 1) {
       finalize(p, d.b, head, ed, o, mc, lc);
+    } else if (kCluster) {
+      // leave this split's (O, m, l) in shared memory, where the cluster's
+      // first CTA reads it after the cluster barrier below
+      named_bar_sync(1, kConsumers);  // every warp is done reading wbuf
+      float* cp = wbuf + eh * kGqaHeadDim + ed;
+      *reinterpret_cast<float4*>(cp) = make_float4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<float4*>(cp + 4) = make_float4(o[4], o[5], o[6], o[7]);
+      if (ed == 0) {
+        wbuf[kGqaPartialFloats + eh] = mc;
+        wbuf[kGqaPartialFloats + kGqaGroup + eh] = lc;
+      }
+      cl_nsplit = d.nsplit;
+      cl_b = d.b;
+      cl_kvh = d.kvh;
     } else {
       // publish this split, then count arrivals in its group of <= 16 splits
       store_partial(p, d.item, eh, ed, o, mc, lc);
@@ -672,27 +701,75 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     named_bar_sync(1, kConsumers);  // wbuf and misc are reused by the next item
   }
+  }  // consumer warps
+
+  if constexpr (kCluster) {
+    // Split merge through distributed shared memory (the Flint page's cluster
+    // reduction): after the first barrier every CTA's partial is visible; the
+    // cluster's first CTA merges them in split order (the result does not
+    // depend on timing) and writes out / lse; the second barrier keeps every
+    // CTA, and so its shared memory, alive until those reads are done.  Every
+    // thread of every CTA reaches both barriers (all earlier waits are bounded).
+    cluster_sync();
+    if (warp < kConsumerWarps && cl_nsplit > 1 && blockIdx.x == 0) {
+      const uint32_t wb0 = smem_u32(wbuf);
+      float o[8], M = -INFINITY, Ls = 0.f;
+      float ms[kGqaMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kGqaMaxCluster; ++r)
+        ms[r] = r < cl_nsplit
+                    ? ld_cluster_f32(map_shared_rank(wb0 + 4u * (kGqaPartialFloats + eh), r))
+                    : -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kGqaMaxCluster; ++r) M = fmaxf(M, ms[r]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = 0.f;
+      const float c2 = p.scale_log2;
+#pragma unroll
+      for (int r = 0; r < kGqaMaxCluster; ++r) {
+        if (r < cl_nsplit) {
+          const uint32_t base_r = map_shared_rank(wb0, r);
+          const float w = (ms[r] == -INFINITY) ? 0.f : ex2((ms[r] - M) * c2);
+          const float lr = ld_cluster_f32(base_r + 4u * (kGqaPartialFloats + kGqaGroup + eh));
+          const float4 a = ld_cluster_f4(base_r + 4u * (eh * kGqaHeadDim + ed));
+          const float4 c = ld_cluster_f4(base_r + 4u * (eh * kGqaHeadDim + ed + 4));
+          Ls = __fmaf_rn(w, lr, Ls);
+          o[0] = __fmaf_rn(w, a.x, o[0]); o[1] = __fmaf_rn(w, a.y, o[1]);
+          o[2] = __fmaf_rn(w, a.z, o[2]); o[3] = __fmaf_rn(w, a.w, o[3]);
+          o[4] = __fmaf_rn(w, c.x, o[4]); o[5] = __fmaf_rn(w, c.y, o[5]);
+          o[6] = __fmaf_rn(w, c.z, o[6]); o[7] = __fmaf_rn(w, c.w, o[7]);
+        }
+      }
+      finalize(p, cl_b, cl_kvh * kGqaGroup + eh, ed, o, M, Ls);
+    }
+    cluster_sync();
+  }
 }
 
-template <int P>
+template <int P, bool kCluster>
 cudaError_t launch_page(const GqaParams& p, const CUtensorMap& kv_map, int grid,
                         cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};
-  const cudaError_t e = set_smem_attr_once(gqa_decode_kernel<P>, kSmemBytes, attr_done);
+  const cudaError_t e =
+      set_smem_attr_once(gqa_decode_kernel<P, kCluster>, kSmemBytes, attr_done);
   if (e != cudaSuccess) return e;
   // launched as a programmatic dependent of the previous kernel on the stream:
-  // its launch and shared-memory setup overlap that kernel's tail
+  // its launch and pre-wait prologue overlap that kernel's tail
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = kCluster ? dim3(p.cluster, p.B * p.Hkv) : dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kCluster ? p.cluster : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gqa_decode_kernel<P>, p, kv_map);
+  cfg.numAttrs = kCluster ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, gqa_decode_kernel<P, kCluster>, p, kv_map);
 }
 
 }  // namespace
@@ -701,8 +778,13 @@ int gqa_ctas_per_sm() { return kCtasPerSm; }
 
 cudaError_t launch_gqa_decode(const GqaParams& p, const CUtensorMap& kv_map, int page_size,
                               int grid, cudaStream_t stream) {
-  return page_size == 16 ? launch_page<16>(p, kv_map, grid, stream)
-                         : launch_page<32>(p, kv_map, grid, stream);
+  if (p.cluster > 1) {
+    if (p.cluster > kGqaMaxCluster) return cudaErrorInvalidValue;
+    return page_size == 16 ? launch_page<16, true>(p, kv_map, grid, stream)
+                           : launch_page<32, true>(p, kv_map, grid, stream);
+  }
+  return page_size == 16 ? launch_page<16, false>(p, kv_map, grid, stream)
+                         : launch_page<32, false>(p, kv_map, grid, stream);
 }
 
 }  // namespace pkv

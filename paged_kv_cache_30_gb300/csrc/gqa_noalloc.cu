@@ -86,7 +86,7 @@ extern "C" PKV_API int pkv_paged_decode_attn_noalloc(
   // The same launch shape as pkv_paged_decode_attn, on the array's limits.
   pkv::GqaShape shape;
   if ((rc = pkv::gqa_launch_shape(call.pairs, call.cap_req, kMaxItems, kMaxPairs, st.num_sms,
-                                  &shape)))
+                                  call.p.max_blocks, call.page_size, &shape)))
     return rc;
 
   pkv::GqaParams& p = call.p;
@@ -98,7 +98,8 @@ extern "C" PKV_API int pkv_paged_decode_attn_noalloc(
   p.part_o = reinterpret_cast<float*>(st.ptr + kCounterInts * 4);
   p.part_ml = p.part_o + kMaxItems * pkv::kGqaPartialFloats;
   p.max_items = kMaxItems;
-  p.cap = shape.cap;
+  p.cap = shape.cluster > 1 ? shape.cluster : shape.cap;
+  p.cluster = shape.cluster;
   p.target_items = shape.target_items;
 
   // The array keeps the previous call's contents: the queue words, the error

@@ -68,11 +68,17 @@ struct GqaParams {
   int* group_counters; // [max_items] arrival counters of split groups (by first item)
   int* sched;
   int* err;
+  int cluster;         // > 1: cluster mode with this many splits per cluster (see below)
 };
 
-// Launch the GQA decode kernel for page size 16 or 32 on `grid` CTAs.
+// Launch the GQA decode kernel for page size 16 or 32.  p.cluster <= 1: the
+// persistent kernel on `grid` CTAs.  p.cluster = C in [2, 8]: the cluster
+// mode, grid (C, B * Hkv) in clusters of C CTAs, CTA r of a cluster taking
+// split r of one (request, kv head); the splits merge through distributed
+// shared memory (no workspace partials, counters or queue).
 cudaError_t launch_gqa_decode(const GqaParams& p, const CUtensorMap& kv_map, int page_size,
                               int grid, cudaStream_t stream);
+constexpr int kGqaMaxCluster = 8;
 int gqa_ctas_per_sm();
 
 // A validated GQA decode call: kernel parameters (without workspace pointers)
@@ -104,9 +110,10 @@ int prepare_gqa_call(const ::pkv_tensor* q, const ::pkv_tensor* kv_cache,
 // the call does not fit.  Every entry point launching the GQA kernel uses it.
 struct GqaShape {
   int cap, grid, target_items;
+  int cluster;  // > 1: cluster mode with this many splits per (request, kv head) at most
 };
 int gqa_launch_shape(int64_t pairs, int cap_req, int64_t max_items, int64_t max_pairs,
-                     int num_sms, GqaShape* shape);
+                     int num_sms, int max_blocks, int page_size, GqaShape* shape);
 // Device address of the error word of pkv_paged_decode_attn_noalloc's static
 // scratch on `device`, or null before that device's first such call.
 int* noalloc_error_word(int device);

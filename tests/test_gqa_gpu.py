@@ -90,21 +90,28 @@ def test_tiny_gqa_config(seed):
     (10, 6, 1, 16, 1, 3000, True, 241, 0),   # widest window whose items never split at P 16
     (11, 6, 1, 16, 1, 3000, True, 242, 0),   # one token wider: the scanning prologue
 ])
-def test_random_cases(seed, B, Hkv, P, Lmin, Lmax, sinks, window, cap):
+@pytest.mark.parametrize("wide", [False, True])
+def test_random_cases(seed, B, Hkv, P, Lmin, Lmax, sinks, window, cap, wide):
+    """wide=False: block tables as wide as the longest request, so small
+    launches whose requests may split take the cluster mode (splits merged
+    through distributed shared memory); wide=True: the same problem with the
+    tables padded to 1024 pages, which keeps the persistent kernel (queue,
+    workspace partials, arrival counters)."""
     prob = W.gqa_problem(seed, B, 8 * Hkv, Hkv, P, "uniform", Lmin, Lmax, sinks=sinks,
-                         window=window, num_kv_splits=cap)
-    check(prob, what=f"case {seed}")
+                         window=window, num_kv_splits=cap, max_blocks=1024 if wide else None)
+    check(prob, what=f"case {seed} wide={wide}")
 
 
 def test_edge_lengths():
     """Empty rows, one key, exact page multiples, one past a page, window 1."""
-    L = np.array([0, 1, 16, 17, 32, 33, 15, 0, 2, 48], dtype=np.int32)
+    L = np.array([0, 1, 16, 17, 32, 33, 15, 0, 2, 48, 300, 257, 256, 513], dtype=np.int32)
     for window in (0, 1, 16, 17, 100):
         for P in (16, 32):
-            prob = W.gqa_problem(11, len(L), 16, 2, P, "const", 1, 64, seq_lens=L, sinks=True,
-                                 window=window)
-            for cap in (1, 3, 0):
-                check(prob, cap, what=f"edge P={P} W={window} cap={cap}")
+            for maxb in (None, 1024):  # cluster mode / persistent kernel
+                prob = W.gqa_problem(11, len(L), 16, 2, P, "const", 1, 513, seq_lens=L,
+                                     sinks=True, window=window, max_blocks=maxb)
+                for cap in (1, 3, 0):
+                    check(prob, cap, what=f"edge P={P} W={window} cap={cap} maxb={maxb}")
 
 
 def test_nan_poisoned_unattended_slots_stay_finite():
@@ -211,12 +218,13 @@ def test_many_calls_leave_counters_at_zero():
     assert np.max(np.abs(out.float().cpu().numpy().reshape(ref_out.shape) - ref_out)) <= TOL_OUT
 
 
-def test_cuda_graph_replay_with_new_lengths_and_tables():
+@pytest.mark.parametrize("maxb", [200, 1024])  # cluster mode / persistent kernel
+def test_cuda_graph_replay_with_new_lengths_and_tables(maxb):
     """The launch shape depends only on the batch: a captured call replays
     correctly after seq_lens and block_table change on the device."""
-    pa = W.gqa_problem(18, 6, 16, 2, 16, "uniform", 1, 2000, sinks=True, max_blocks=200,
+    pa = W.gqa_problem(18, 6, 16, 2, 16, "uniform", 1, 2000, sinks=True, max_blocks=maxb,
                        pool_pages=1200)
-    pb = W.gqa_problem(19, 6, 16, 2, 16, "uniform", 1, 3000, sinks=True, max_blocks=200,
+    pb = W.gqa_problem(19, 6, 16, 2, 16, "uniform", 1, 3000, sinks=True, max_blocks=maxb,
                        pool_pages=1200)
     pb.q = pa.q
     pb.sinks = pa.sinks
@@ -262,12 +270,14 @@ def test_calls_on_two_streams_are_ordered():
 
 # --------------------------------------------------------- input errors --
 
-def test_bad_block_table_entry_is_flagged_not_faulted():
-    prob = W.gqa_problem(21, 3, 8, 1, 16, "const", 100, 100)
+@pytest.mark.parametrize("L", [100, 600])  # persistent kernel / cluster mode (3 splits)
+def test_bad_block_table_entry_is_flagged_not_faulted(L):
+    prob = W.gqa_problem(21, 3, 8, 1, 16, "const", L, L)
     bt = prob.block_table.clone()
     nb = prob.kv_cache.shape[0]
     bt[1, 2] = nb + 5          # past the end of the cache
     bt[2, 0] = -1              # unassigned entry inside the attended range
+    bt[0, L // 16 - 1] = nb    # the last page of a later split
     q, kv, sl = dev(prob.q), dev(prob.kv_cache), dev(prob.seq_lens)
     out = torch.empty_like(q)
     pkv.paged_decode_attn(q, kv, bt.cuda(), sl, None, 0, prob.scale, 16, 0, out, None)
@@ -278,11 +288,13 @@ def test_bad_block_table_entry_is_flagged_not_faulted():
     check(prob, what="after bad table")
 
 
-@pytest.mark.parametrize("window, cap", [(0, 0), (128, 0), (0, 1)])
-def test_seq_len_beyond_block_table_is_flagged(window, cap):
+@pytest.mark.parametrize("window, cap, maxb", [(0, 0, 4), (128, 0, 4), (0, 1, 4), (0, 0, 40),
+                                               (0, 3, 40)])
+def test_seq_len_beyond_block_table_is_flagged(window, cap, maxb):
     # (128, 0) and (0, 1): no request can split, so the kernel skips the
-    # scanning prologue and checks the lengths as it decodes each item
-    prob = W.gqa_problem(22, 2, 8, 1, 16, "const", 64, 64, max_blocks=4)
+    # scanning prologue and checks the lengths as it decodes each item;
+    # maxb 40: the cluster mode checks them as it decodes its split
+    prob = W.gqa_problem(22, 2, 8, 1, 16, "const", 64, 64, max_blocks=maxb)
     sl = prob.seq_lens.clone()
     sl[0] = 1000
     out = torch.empty_like(dev(prob.q))
