@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
 SOURCES = ["api.cpp", "gqa_decode.cu", "gqa_noalloc.cu", "mla_verify.cu", "mla_verify_native.cu",
-           "kv_append.cu"]
+           "mla_verify_pair.cu", "kv_append.cu"]
 HEADERS = ["pkv_internal.h", "ptx.cuh", "tcgen05.cuh", "mla_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",

@@ -602,7 +602,10 @@ static int mla_verify_impl(const pkv_tensor* q, const pkv_tensor* q8, const pkv_
 
   EncodeTiledFn encode = nullptr;
   if ((rc = get_encoder(&encode))) return rc;
-  CUtensorMap q_map, kv_map;
+  CUtensorMap q_map, kv_map, v_map;
+  // bf16 cache and an even number of verify tokens: tokens 2tp and 2tp + 1
+  // share every key tile on a CTA pair
+  const bool pair = !native && !fp8 && qlen % 2 == 0;
   if (native) {
     // the e4m3 cache as (64 dims, tokens, 9 chunks of 64 dims, pages): a box of
     // (64, 8, 9, 1) lands chunk-major, 8 rows of 64 bytes per chunk, 64-byte swizzle
@@ -642,6 +645,19 @@ static int mla_verify_impl(const pkv_tensor* q, const pkv_tensor* q8, const pkv_
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (cr != CUDA_SUCCESS)
         return fail(PKV_ERR_INVALID_ARG, "latent cache tensor map rejected (%d)", (int)cr);
+    }
+    if (pair) {
+      // the same view, boxes of 16 tokens x 2 chunks: 128 V dims of 16 keys,
+      // landing chunk-major (two 2 KB slabs of 16 rows of 128 bytes)
+      const cuuint64_t gdim[4] = {64, cuuint64_t(page_size), 9, cuuint64_t(num_pages)};
+      const cuuint64_t gstr[3] = {cuuint64_t(s_tok) * 2, 128, cuuint64_t(s_page) * 2};
+      const cuuint32_t box[4] = {64, 16, 2, 1};
+      const cuuint32_t es[4] = {1, 1, 1, 1};
+      CUresult cr = encode(&v_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, latent_cache->data, gdim,
+                           gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (cr != CUDA_SUCCESS)
+        return fail(PKV_ERR_INVALID_ARG, "latent cache V tensor map rejected (%d)", (int)cr);
     }
   }
   pkv::MlaParams p;
@@ -688,6 +704,7 @@ static int mla_verify_impl(const pkv_tensor* q, const pkv_tensor* q8, const pkv_
   if ((rc = order_streams(st, stream, capturing))) return rc;
   const cudaError_t e =
       native ? pkv::launch_mla_verify_native(p, kv_map, int(units * cap), stream)
+      : pair ? pkv::launch_mla_verify_pair(p, q_map, kv_map, v_map, int(units * cap), stream)
              : pkv::launch_mla_verify(p, q_map, kv_map, fp8, int(units * cap), stream);
   if (e != cudaSuccess) return cuda_fail(e, "mla verify launch");
   return PKV_OK;

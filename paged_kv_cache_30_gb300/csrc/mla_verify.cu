@@ -609,16 +609,18 @@ constexpr int kPlanThreads = 1024;
 constexpr int kPlanSortMax = 8192;
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
-    mla_plan_kernel(const __grid_constant__ MlaParams p, int grid) {
+    mla_plan_kernel(const __grid_constant__ MlaParams p, int grid, int pair) {
   griddep_wait();
   griddep_launch_dependents();
   extern __shared__ unsigned long long keys[];  // [P2] (length, request) sort keys
   __shared__ int warp_sums[kPlanThreads / 32];
   __shared__ int s_total;
   const int B = p.B, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int per_split = p.qlen * 2;
+  // one entry per CTA (row t = verify token), or per CTA pair (t = token pair)
+  const int rows = pair ? p.qlen / 2 : p.qlen;
+  const int per_split = rows * 2;
   auto entry = [&](int b, int split, int t, int half) {
-    return (((b * p.qlen + t) * 2 + half) << 4) | split;
+    return (((b * rows + t) * 2 + half) << 4) | split;
   };
   if (B > kPlanSortMax) {  // request order, a fixed slot per (request, split)
     for (int x = tid; x < grid; x += kPlanThreads) {
@@ -710,7 +712,7 @@ cudaError_t launch_t(const MlaParams& p, const CUtensorMap& q_map, const CUtenso
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = set_smem_attr_once(mla_verify_kernel<kFp8>, Cfg<kFp8>::kSmemBytes, attr_done);
   if (e != cudaSuccess) return e;
-  e = launch_mla_plan(p, grid, stream);
+  e = launch_mla_plan(p, grid, stream, false);
   if (e != cudaSuccess) return e;
   return launch_pdl(mla_verify_kernel<kFp8>, grid, Cfg<kFp8>::kThreads, Cfg<kFp8>::kSmemBytes,
                     stream, p, q_map, kv_map);
@@ -718,14 +720,14 @@ cudaError_t launch_t(const MlaParams& p, const CUtensorMap& q_map, const CUtenso
 
 }  // namespace
 
-cudaError_t launch_mla_plan(const MlaParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_mla_plan(const MlaParams& p, int grid, cudaStream_t stream, bool pair) {
   static std::atomic<uint64_t> plan_attr_done{0};
   cudaError_t e = set_smem_attr_once(mla_plan_kernel, kPlanSortMax * 8, plan_attr_done);
   if (e != cudaSuccess) return e;
   int p2 = 1;
   while (p2 < p.B) p2 <<= 1;
   return launch_pdl(mla_plan_kernel, 1, kPlanThreads, p.B > kPlanSortMax ? 0 : p2 * 8, stream, p,
-                    grid);
+                    grid, pair ? 1 : 0);
 }
 
 cudaError_t launch_mla_verify(const MlaParams& p, const CUtensorMap& q_map,

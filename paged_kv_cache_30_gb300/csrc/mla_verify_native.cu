@@ -599,7 +599,7 @@ cudaError_t launch_mla_verify_native(const MlaParams& p, const CUtensorMap& kv_m
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = set_smem_attr_once(mla_verify_native_kernel, kSmemBytes, attr_done);
   if (e != cudaSuccess) return e;
-  e = launch_mla_plan(p, grid, stream);
+  e = launch_mla_plan(p, grid, stream, false);
   if (e != cudaSuccess) return e;
   return launch_pdl(mla_verify_native_kernel, grid, kThreads, kSmemBytes, stream, p, kv_map);
 }

@@ -159,8 +159,16 @@ struct MlaParams {
   int64_t qs_sr, qs_sh;
 };
 
-// The planning kernel: writes p.plan[0, grid) (one CTA; programmatic dependent launch).
-cudaError_t launch_mla_plan(const MlaParams& p, int grid, cudaStream_t stream);
+// The planning kernel: writes p.plan[0, grid) (one CTA; programmatic dependent
+// launch): one entry per verify CTA, or with `pair` one per CTA pair (a pair
+// takes two consecutive verify tokens).
+cudaError_t launch_mla_plan(const MlaParams& p, int grid, cudaStream_t stream, bool pair);
+// bf16 latent cache, even qlen: the planning kernel, then the verify kernel on
+// CTA pairs (grid CTAs, clusters of 2; v_map: the cache as (64 dims, token,
+// 9 chunks, page) with a box of (64, 16, 2, 1), 128-byte swizzle).
+cudaError_t launch_mla_verify_pair(const MlaParams& p, const CUtensorMap& q_map,
+                                   const CUtensorMap& kv_map, const CUtensorMap& v_map, int grid,
+                                   cudaStream_t stream);
 cudaError_t launch_mla_verify(const MlaParams& p, const CUtensorMap& q_map,
                               const CUtensorMap& kv_map, bool fp8, int grid, cudaStream_t stream);
 // Native FP8: planning kernel, then the verify kernel with S = Q8 K8^T on

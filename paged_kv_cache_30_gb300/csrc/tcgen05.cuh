@@ -136,6 +136,59 @@ __device__ __forceinline__ void commit(uint32_t mbar_smem) {
       : "memory");
 }
 
+// ------------------------------------------------------ CTA pairs (2 SMs) --
+// The cta_group::2 forms, for a cluster of two CTAs that share each MMA: a
+// kernel uses either these or the cta_group::1 forms above, never both.
+// Allocation and deallocation are collective: one warp of each CTA of the pair
+// executes them (both receive the same TMEM address).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D (+)= A * B over the pair, issued by one elected lane of the even CTA:
+// M = 256 rows, rows 0..127 from the even CTA's A (and D in its TMEM), rows
+// 128..255 from the odd CTA's A (D in its TMEM, same address); B's N columns
+// come half from each CTA's shared memory at the same descriptor address
+// (first half from the even CTA).  A from shared memory:
+__device__ __forceinline__ void mma_pair_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                  uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+// ... and A from each CTA's TMEM (same address in both).
+__device__ __forceinline__ void mma_pair_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                  uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+// Arrive once on the mbarrier at offset `mbar_smem` of every CTA of the pair
+// when the pair's MMAs issued so far are done (one elected lane issues).
+__device__ __forceinline__ void commit_pair_elect(uint32_t mbar_smem) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(mbar_smem),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
 // -------------------------------------------------------- TMEM load/store --
 // 32 lanes x 32 bit, 32 consecutive columns: thread i of the warp gets lane
 // (base lane + i), columns [col, col + 32).  A warp may only touch the 32-lane
