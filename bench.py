@@ -732,7 +732,7 @@ def run_gpu(args, rank, world, local_rank):
         "hbm_frac_of_nominal_8tbs": value / 8000.0,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(),
-                     "kernel": "gqa_decode_kernel<16> (full-attention layer)",
+                     "kernel": "gqa_decode_kernel<16, 0> (persistent mode, full-attention layer)",
                      "peak_source": f"{peak_kind} hbm_gbs", "launch_ms": full_mean,
                      "timing": "mean of one event pair around each full-layer launch over "
                                "K steps timed after the value loop (those steps: "
