@@ -63,6 +63,12 @@ static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0 &&
                   kKBytes % 1024 == 0 && kVBytes % 1024 == 0,
               "swizzle atoms need 1024 B alignment");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+// At a unit's start the query dims [0, 384) land by TMA in a staging area over
+// key slot 2, the V ring and P (free until the first tiles are consumed).
+constexpr int kOffStaging = kOffK + 2 * kKBytes;
+constexpr int kQtBytes = kQtChunks * kQChunkBytes;       // 98304
+static_assert(kOffStaging + kQtBytes <= kOffP + kPBytes && kOffStaging % 1024 == 0,
+              "query staging area");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
@@ -74,8 +80,8 @@ constexpr float kRescaleLog2 = 8.0f;
 // barriers (same offsets in both CTAs; the ones marked "even" are used in
 // the even CTA only, with arrivals from both)
 enum {
-  kQFull = 0,     // this CTA's query dims 384..575 landed (TMA)
-  kQtReady = 1,   // this CTA's query dims 0..383 stored into TMEM (256 arrivals)
+  kQFull = 0,     // this CTA's query landed (TMA: dims 384..575, and 0..383 staged)
+  kQtReady = 1,   // query dims 0..383 moved from staging into TMEM (256 arrivals)
   kQReady = 2,    // even: both CTAs' query ready (2 arrivals)
   kKFull = 3,     // even: key slot s of both CTAs landed (2 arrivals + bytes), 3 slots
   kKEmpty = 6,    // key slot s free (pair commit after S), 3 slots
@@ -187,9 +193,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n > 0) {
       const int qrow = u.b * p.qlen + u.t;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(kQFull), kQsBytes);
+        mbar_arrive_expect_tx(bar(kQFull), kQsBytes + kQtBytes);
         for (int c = 0; c < kQsChunks; ++c)
           tma_load_3d(sQ + c * kQChunkBytes, &q_map, bar(kQFull), 64 * (kQtChunks + c), 0, qrow);
+        for (int c = 0; c < kQtChunks; ++c)
+          tma_load_3d(base_u32 + kOffStaging + c * kQChunkBytes, &q_map, bar(kQFull), 64 * c, 0,
+                      qrow);
       }
       const int32_t* bt_row = p.bt + (long long)u.b * p.bt_sb;
       const int vchunk = 4 * u.half + 2 * (int)rank;
@@ -206,25 +215,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = g; i < min(n, g + 8); ++i) {
           const int j = 4 * (i - g);
-          int pb[4], po[4];
+          int pb[4], po[4], pb1[4], po1[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             pb[q] = __shfl_sync(0xffffffffu, blk, j + q);
             po[q] = __shfl_sync(0xffffffffu, off, j + q);
+            pb1[q] = __shfl_sync(0xffffffffu, blk, (j + 4 + q) & 31);  // tile i + 1 (used at i == 0)
+            po1[q] = __shfl_sync(0xffffffffu, off, (j + 4 + q) & 31);
           }
           if (lane == 0) {
-            const int st = i % kStages;
             // this CTA's 32 keys: pieces 2 rank, 2 rank + 1, two 8-key boxes each
-            mbar_wait(bar(kKEmpty + st), ((i / kStages) & 1) ^ 1u, p.err);
-            const uint32_t full = even_bar(kKFull + st);
-            mbar_arrive_expect_tx_cluster(full, kKBytes);
-            const uint32_t dk = sK(st);
-            const int h0 = 2 * (int)rank, h1 = h0 + 1;
-            tma_load_4d_pair(dk, &kv_map, full, 0, po[h0], 0, pb[h0]);
-            tma_load_4d_pair(dk + kGroupBytes, &kv_map, full, 0, po[h0] + 8, 0, pb[h0]);
-            tma_load_4d_pair(dk + 2 * kGroupBytes, &kv_map, full, 0, po[h1], 0, pb[h1]);
-            tma_load_4d_pair(dk + 3 * kGroupBytes, &kv_map, full, 0, po[h1] + 8, 0, pb[h1]);
+            auto issue_k = [&](int t, const int (&b)[4], const int (&o)[4]) {
+              const int sk = t % kStages;
+              mbar_wait(bar(kKEmpty + sk), ((t / kStages) & 1) ^ 1u, p.err);
+              const uint32_t full = even_bar(kKFull + sk);
+              mbar_arrive_expect_tx_cluster(full, kKBytes);
+              const uint32_t dk = sK(sk);
+              const int h0 = 2 * (int)rank, h1 = h0 + 1;
+              tma_load_4d_pair(dk, &kv_map, full, 0, o[h0], 0, b[h0]);
+              tma_load_4d_pair(dk + kGroupBytes, &kv_map, full, 0, o[h0] + 8, 0, b[h0]);
+              tma_load_4d_pair(dk + 2 * kGroupBytes, &kv_map, full, 0, o[h1], 0, b[h1]);
+              tma_load_4d_pair(dk + 3 * kGroupBytes, &kv_map, full, 0, o[h1] + 8, 0, b[h1]);
+            };
+            if (i != 1) issue_k(i, pb, po);  // key tile 1 goes out with tile 0
+            if (i == 0) {
+              if (n > 1) issue_k(1, pb1, po1);
+              // key slot 2, the V ring and P held the staged query until it
+              // was moved into TMEM
+              mbar_wait(bar(kQtReady), 0, p.err);
+            }
             // all 64 keys of this CTA's 128 V dims: box q = keys 16q.., 2 chunks
+            const int st = i % kStages;
             mbar_wait(bar(kVEmpty + st), ((i / kStages) & 1) ^ 1u, p.err);
             mbar_arrive_expect_tx(bar(kVFull + st), kVBytes);
             const uint32_t dv = sV(st);
@@ -305,26 +326,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * quarter + lane;  // head = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     if (n > 0) {
-      // query dims [0, 384) into TMEM: this warp writes lanes 32 quarter ..,
-      // chunks 3 chalf .. + 2 (24 16-byte loads a thread)
+      // query dims [0, 384) from the staging area into TMEM: this warp writes
+      // lanes 32 quarter .., chunks 3 chalf .. + 2 (row `row` of each 16 KB
+      // chunk, 128-byte swizzle: 16-byte unit k at k ^ (row % 8))
       const int c0 = 3 * chalf;
-      const uint4* qsrc = reinterpret_cast<const uint4*>(
-          p.q + ((long long)u.b * p.qlen + u.t) * p.q_sr + (long long)row * p.q_sh) + 8 * c0;
-      uint4 w[24];
-#pragma unroll
-      for (int k = 0; k < 24; ++k) w[k] = __ldg(qsrc + k);
+      mbar_wait(bar(kQFull), 0, p.err);
+      const uint8_t* stg = base + kOffStaging + (row / 8) * 1024 + (row % 8) * 128;
 #pragma unroll
       for (int j = 0; j < 3; ++j) {
         uint32_t v[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          v[4 * k] = w[8 * j + k].x;
-          v[4 * k + 1] = w[8 * j + k].y;
-          v[4 * k + 2] = w[8 * j + k].z;
-          v[4 * k + 3] = w[8 * j + k].w;
+          const uint4 w = *reinterpret_cast<const uint4*>(stg + (c0 + j) * kQChunkBytes +
+                                                          ((k ^ (row % 8)) * 16));
+          v[4 * k] = w.x;
+          v[4 * k + 1] = w.y;
+          v[4 * k + 2] = w.z;
+          v[4 * k + 3] = w.w;
         }
         tc::st_32x32b_x32(tmem + lane_base + kTmemQ + 32 * (c0 + j), v);
       }
+      fence_proxy_async_smem();  // the staging area is refilled by TMA after this
       tc::wait_st();
       tc::fence_before_sync();
       mbar_arrive(bar(kQtReady));
