@@ -82,9 +82,15 @@ struct Cfg {
   static constexpr int kOffP = kOffF8 + kF8Stages * kF8StageBytes;
   static constexpr int kOffBars = kOffP + kPBytes;
   static constexpr int kSmemBytes = kOffBars + 256 + 1024;
+  // At a unit's start the query dims [0, 384) land by TMA in a staging area
+  // over bf16 stages 1..3 (bf16 cache: stage 0 takes the first tile at once)
+  // or 0..2 (FP8: the e4m3 ring takes the first tiles; the converters wait).
+  static constexpr int kOffStaging = kFp8 ? kOffStages : kOffStages + kStageBytes;
+  static constexpr int kQtBytes = kQtChunks * kQChunkBytes;  // 98304
   static_assert(kOffStages % 1024 == 0 && kOffF8 % 1024 == 0 && kOffP % 1024 == 0,
                 "swizzle atoms need 1024 B alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kOffStaging + kQtBytes <= (kFp8 ? kOffF8 : kOffP), "query staging area");
 };
 
 constexpr uint32_t kTmemCols = 512;
@@ -163,27 +169,30 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 
   // Query dims [0, 384) into TMEM (the A operand of the first 24 K16 steps of
   // S = Q K^T), shared by warps 0..7: warp w writes TMEM lanes (heads)
-  // 32 (w % 4) .. + 31, 64-dim chunks 3 (w / 4) .. + 2, one round of 24
-  // 16-byte loads per thread; 256 arrivals on kQtReady.
+  // 32 (w % 4) .. + 31, 64-dim chunks 3 (w / 4) .. + 2, read from the staging
+  // area the producer's TMA filled (row = head of each 16 KB chunk, 128-byte
+  // swizzle: 16-byte unit k at k ^ (head % 8)); 256 arrivals on kQtReady, after
+  // which the staging area may be refilled.  (Per-thread global loads at a
+  // 1152-byte lane stride took ~8 us here.)
   auto load_qt_share = [&]() {
     const int head = 32 * (warp & 3) + lane, c0 = 3 * ((warp >> 2) & 1);
-    const uint4* qsrc = reinterpret_cast<const uint4*>(
-        p.q + ((long long)u.b * p.qlen + u.t) * p.q_sr + (long long)head * p.q_sh) + 8 * c0;
-    uint4 w[24];
-#pragma unroll
-    for (int k = 0; k < 24; ++k) w[k] = __ldg(qsrc + k);
+    mbar_wait(bar(kQFull), 0, p.err);
+    const uint8_t* stg = base + C::kOffStaging + (head / 8) * 1024 + (head % 8) * 128;
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
       uint32_t v[32];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        v[4 * k] = w[8 * j + k].x;
-        v[4 * k + 1] = w[8 * j + k].y;
-        v[4 * k + 2] = w[8 * j + k].z;
-        v[4 * k + 3] = w[8 * j + k].w;
+        const uint4 w =
+            *reinterpret_cast<const uint4*>(stg + (c0 + j) * kQChunkBytes + ((k ^ (head % 8)) * 16));
+        v[4 * k] = w.x;
+        v[4 * k + 1] = w.y;
+        v[4 * k + 2] = w.z;
+        v[4 * k + 3] = w.w;
       }
       tc::st_32x32b_x32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kTmemQ + 32 * (c0 + j), v);
     }
+    fence_proxy_async_smem();  // the staging area is refilled by the async proxy
     tc::wait_st();
     tc::fence_before_sync();
     mbar_arrive(bar(kQtReady));
@@ -194,9 +203,12 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     if (n > 0) {
       const int qrow = u.b * p.qlen + u.t;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(kQFull), kQsBytes);
+        mbar_arrive_expect_tx(bar(kQFull), kQsBytes + C::kQtBytes);
         for (int c = 0; c < kQsChunks; ++c)
           tma_load_3d(sQ + c * kQChunkBytes, &q_map, bar(kQFull), 64 * (kQtChunks + c), 0, qrow);
+        for (int c = 0; c < kQtChunks; ++c)
+          tma_load_3d(base_u32 + C::kOffStaging + c * kQChunkBytes, &q_map, bar(kQFull), 64 * c, 0,
+                      qrow);
       }
       const int32_t* bt_row = p.bt + (long long)u.b * p.bt_sb;
       // lane l holds the block id / page offset of 16-key piece l of the tiles
@@ -217,8 +229,13 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
         int blk, off;
         piece(g, blk, off);
         for (int i = g; i < min(n, g + 16); ++i) {
-          // the ring's first fill needs no wait: the query share comes after it
-          if (i == min(n, kFp8 ? C::kF8Ring : kStages)) load_qt_share();
+          // bf16: stage 0 needs no wait; stages 1..3 held the staged query, so
+          // the producer first moves its share and waits for everyone's.
+          // FP8: the e4m3 ring is outside the staging area.
+          if (kFp8 ? i == min(n, C::kF8Ring) : i == 1) {
+            load_qt_share();
+            if (!kFp8) mbar_wait(bar(kQtReady), 0, p.err);
+          }
           const int b0 = __shfl_sync(0xffffffffu, blk, 2 * (i - g));
           const int o0 = __shfl_sync(0xffffffffu, off, 2 * (i - g));
           const int b1 = __shfl_sync(0xffffffffu, blk, 2 * (i - g) + 1);
@@ -248,7 +265,7 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
           }
         }
       }
-      if (n <= (kFp8 ? C::kF8Ring : kStages)) load_qt_share();
+      if (n <= (kFp8 ? C::kF8Ring : 1)) load_qt_share();
     }
   } else if (warp == 1) {
     // ============================= MMA issuer =============================
@@ -312,6 +329,8 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
     // and to the output instead.
     const int ct = (warp < 8) ? tid - 64 : tid - 256 + 64;  // 0 .. 191
     if (warp < 8 && n > 0) load_qt_share();
+    // the bf16 stages held the staged query
+    if (n > 0) mbar_wait(bar(kQtReady), 0, p.err);
     for (int i = 0; i < n; ++i) {
       const int sf = i % C::kF8Ring, st = i % kStages;
       mbar_wait(bar(kF8Full + sf), (i / C::kF8Ring) & 1, p.err);
