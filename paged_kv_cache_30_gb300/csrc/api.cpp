@@ -457,6 +457,7 @@ PKV_API int pkv_paged_decode_attn(const pkv_tensor* q, const pkv_tensor* kv_cach
   pkv::GqaParams& p = call.p;
   p.cap = shape.cluster > 1 ? shape.cluster : shape.cap;
   p.cluster = shape.cluster;
+  p.min_pages = shape.min_pages;
   p.target_items = shape.target_items;
   p.part_o = ws.partials;
   p.part_ml = ws.partials + max_items * pkv::kGqaPartialFloats;
@@ -1051,7 +1052,6 @@ int prepare_gqa_call(const pkv_tensor* q, const pkv_tensor* kv_cache,
   p.window = window;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.scale = scale;
-  p.min_pages = 256 / page_size;  // a split streams at least 256 tokens (128 KB per kv head)
   return PKV_OK;
 }
 
@@ -1079,18 +1079,25 @@ int gqa_launch_shape(int64_t pairs, int cap_req, int64_t max_items, int64_t max_
   // single 16-way level (one 131072-token request, auto cap, on GB300:
   // 118.7 -> 106.5 us; eight of them 632.8 -> 627.4 us).
   shape->target_items = int(std::max<int64_t>(grid, std::min<int64_t>(grid * 4, pairs * 16)));
-  // Cluster mode (splits merged through distributed shared memory, no queue
-  // and no workspace partials) for small launches whose requests are short:
+  // A split streams at least 256 keys (128 KB per kv head).  Cluster mode
+  // (splits merged through distributed shared memory, no queue and no
+  // workspace partials) for small launches whose requests are short:
   // C = splits a request of the block table's full width can use (at most 8,
-  // at least 256 keys each), when every (request, kv head) gets its own
-  // cluster in a single wave and no split can exceed 64 pages.
-  const int64_t min_pages = 256 / page_size;
-  const int64_t c = std::min<int64_t>(
-      std::min<int64_t>(cap, kGqaMaxCluster), (int64_t(max_blocks) + min_pages - 1) / min_pages);
+  // at least 128 keys each: then a CTA's whole split is usually among the
+  // tiles it requests before the dependency wait; A/B on the tiny batch,
+  // graph-replayed: 256 -> 128 keys 5.4 -> 4.0 us per call, 64 keys no
+  // better), when every (request, kv head) gets its own cluster in a single
+  // wave and no split can exceed 64 pages.
+  shape->min_pages = 256 / page_size;
+  const int64_t cl_min = 128 / page_size;
+  const int64_t c = std::min<int64_t>(std::min<int64_t>(cap, kGqaMaxCluster),
+                                      (int64_t(max_blocks) + cl_min - 1) / cl_min);
   shape->cluster = 0;
   if (c >= 2 && c * pairs <= int64_t(num_sms) * gqa_ctas_per_sm() &&
-      (int64_t(max_blocks) + c - 1) / c <= 64)
+      (int64_t(max_blocks) + c - 1) / c <= 64) {
     shape->cluster = int(c);
+    shape->min_pages = int(cl_min);
+  }
   return PKV_OK;
 }
 

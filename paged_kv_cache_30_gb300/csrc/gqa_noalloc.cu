@@ -100,6 +100,7 @@ extern "C" PKV_API int pkv_paged_decode_attn_noalloc(
   p.max_items = kMaxItems;
   p.cap = shape.cluster > 1 ? shape.cluster : shape.cap;
   p.cluster = shape.cluster;
+  p.min_pages = shape.min_pages;
   p.target_items = shape.target_items;
 
   // The array keeps the previous call's contents: the queue words, the error

@@ -110,7 +110,8 @@ int prepare_gqa_call(const ::pkv_tensor* q, const ::pkv_tensor* kv_cache,
 // the call does not fit.  Every entry point launching the GQA kernel uses it.
 struct GqaShape {
   int cap, grid, target_items;
-  int cluster;  // > 1: cluster mode with this many splits per (request, kv head) at most
+  int cluster;    // > 1: cluster mode with this many splits per (request, kv head) at most
+  int min_pages;  // fewest pages a split may hold
 };
 int gqa_launch_shape(int64_t pairs, int cap_req, int64_t max_items, int64_t max_pairs,
                      int num_sms, int max_blocks, int page_size, GqaShape* shape);
