@@ -59,9 +59,10 @@
  *    Before waiting for it, pkv_paged_decode_attn (and its no-alloc variant)
  *    reads seq_lens, block_table and up to 8 tiles of the leading KV pages of
  *    each CTA's first work item -- never the page holding position
- *    seq_len - 1.  So seq_lens, block_table and the cache pages before the
- *    current token's must not be written by a kernel that may still be running
- *    when the call's kernel starts (the kernel immediately before it on the
+ *    seq_len - 1; the MLA verify calls' planning kernel reads seq_lens.  So
+ *    seq_lens, block_table and the cache pages before the current token's
+ *    must not be written by a kernel that may still be running when the
+ *    call's kernel starts (the kernel immediately before it on the
  *    stream, or one an earlier dependent launch let run early).  Writing the
  *    current token's slot right before the call (pkv_gqa_kv_append) is fine,
  *    as is anything written by copies or by kernels that completed.  q, sinks,

@@ -696,6 +696,7 @@ static int mla_verify_impl(const pkv_tensor* q, const pkv_tensor* q8, const pkv_
   p.cap = int(cap);
   p.page_size = page_size;
   p.scale = scale;
+  p.pair_slots = ws.num_sms / 2;
   p.partials = ws.partials;
   p.max_slots = max_slots;
   p.counters = ws.counters;

@@ -20,22 +20,30 @@ __device__ __forceinline__ int clamped_len(const MlaParams& p, int b) {
   return L;
 }
 
-__device__ __forceinline__ int split_count(const MlaParams& p, int L) {
+// Splits of a request of L keys when a split holds at least min_tiles tiles
+// (at most p.cap; the planning kernel picks min_tiles and writes the count
+// into every entry, so the verify kernels never recompute it).
+__device__ __forceinline__ int split_count(const MlaParams& p, int L, int min_tiles) {
   const int req_tiles = (L + kMlaTile - 1) / kMlaTile;
-  const int ns = (req_tiles + kMlaMinTiles - 1) / kMlaMinTiles;
+  const int ns = (req_tiles + min_tiles - 1) / min_tiles;
   return ns < 1 ? 1 : (ns > p.cap ? p.cap : ns);
 }
 
 // Tiles of the largest split of a request of L keys.
-__device__ __forceinline__ int split_tiles(const MlaParams& p, int L) {
+__device__ __forceinline__ int split_tiles(const MlaParams& p, int L, int min_tiles) {
   const int req_tiles = (L + kMlaTile - 1) / kMlaTile;
-  const int ns = split_count(p, L);
+  const int ns = split_count(p, L, min_tiles);
   return (req_tiles + ns - 1) / ns;
 }
 
-// The unit of this CTA, from the plan the planning kernel wrote: entry
-// ((b * qlen + t) * 2 + half) * 16 + split, or -1 (returned as split 0 of
-// nsplit 0: no unit).
+// Plan entry of (request b, row t, half, split of nsplit): row t is a verify
+// token, or a token pair for CTA-pair launches; split, nsplit - 1 < 16.
+__device__ __forceinline__ int plan_entry(int rows, int b, int t, int half, int split, int nsplit) {
+  return ((((b * rows + t) * 2 + half) << 4 | split) << 4) | (nsplit - 1);
+}
+
+// The unit of this CTA, from the plan the planning kernel wrote (see
+// plan_entry), or -1 (returned as split 0 of nsplit 0: no unit).
 __device__ __forceinline__ Unit decode_unit(const MlaParams& p) {
   Unit u;
   const int v = __ldg(p.plan + blockIdx.x);
@@ -44,8 +52,9 @@ __device__ __forceinline__ Unit decode_unit(const MlaParams& p) {
     u.nsplit = 0;
     return u;
   }
-  u.split = v & 15;
-  const int ch = v >> 4;
+  u.split = (v >> 4) & 15;
+  const int ns = (v & 15) + 1;
+  const int ch = v >> 8;
   u.half = ch & 1;
   const int rt = ch >> 1;
   u.b = rt / p.qlen;
@@ -58,7 +67,6 @@ __device__ __forceinline__ Unit decode_unit(const MlaParams& p) {
   u.L = L;
   u.lim = lim;
   const int req_tiles = (L + kMlaTile - 1) / kMlaTile;
-  const int ns = split_count(p, L);
   u.nsplit = ns;
   const int a = (int)((long long)req_tiles * u.split / ns);
   const int e = (int)((long long)req_tiles * (u.split + 1) / ns);

@@ -629,7 +629,9 @@ constexpr int kPlanSortMax = 8192;
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
     mla_plan_kernel(const __grid_constant__ MlaParams p, int grid, int pair) {
-  griddep_wait();
+  // Before the dependency wait only seq_lens is read (complete before the
+  // kernel this launch depends on, like the block table); the plan, which the
+  // previous call's verify kernel may still be reading, is written after it.
   griddep_launch_dependents();
   extern __shared__ unsigned long long keys[];  // [P2] (length, request) sort keys
   __shared__ int warp_sums[kPlanThreads / 32];
@@ -638,15 +640,38 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   // one entry per CTA (row t = verify token), or per CTA pair (t = token pair)
   const int rows = pair ? p.qlen / 2 : p.qlen;
   const int per_split = rows * 2;
-  auto entry = [&](int b, int split, int t, int half) {
-    return (((b * rows + t) * 2 + half) << 4) | split;
+  // the minimum split: CTA pairs take the wider one when the batch still has
+  // a unit for every CTA pair at that size
+  int min_tiles = kMlaMinTiles;
+  if (pair) {
+    int mine = 0;
+    for (int b = tid; b < B; b += kPlanThreads)
+      mine += split_count(p, clamped_len(p, b), kMlaMinTilesWide);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+    if (lane == 0) warp_sums[wid] = mine;
+    __syncthreads();
+    if (wid == 0) {
+      int v = warp_sums[lane];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == 0) s_total = v;
+    }
+    __syncthreads();
+    if ((long long)s_total * per_split >= p.pair_slots) min_tiles = kMlaMinTilesWide;
+    __syncthreads();  // warp_sums and s_total are reused below
+  }
+  auto entry = [&](int b, int split, int ns, int t, int half) {
+    return plan_entry(rows, b, t, half, split, ns);
   };
   if (B > kPlanSortMax) {  // request order, a fixed slot per (request, split)
+    griddep_wait();
     for (int x = tid; x < grid; x += kPlanThreads) {
       const int per_b = p.cap * per_split;
       const int b = x / per_b, rem = x - b * per_b;
       const int split = rem / per_split, th = rem - split * per_split;
-      p.plan[x] = split < split_count(p, clamped_len(p, b)) ? entry(b, split, th >> 1, th & 1) : -1;
+      const int ns = split_count(p, clamped_len(p, b), min_tiles);
+      p.plan[x] = split < ns ? entry(b, split, ns, th >> 1, th & 1) : -1;
     }
     return;
   }
@@ -655,7 +680,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   for (int i = tid; i < P2; i += kPlanThreads) {
     unsigned long long k = ~0ull;
     if (i < B)
-      k = ((unsigned long long)(0x7fffffff - split_tiles(p, clamped_len(p, i))) << 32) | (unsigned)i;
+      k = ((unsigned long long)(0x7fffffff - split_tiles(p, clamped_len(p, i), min_tiles)) << 32) |
+          (unsigned)i;
     keys[i] = k;
   }
   __syncthreads();
@@ -678,7 +704,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   const int r0 = min(B, tid * R), r1 = min(B, r0 + R);
   int mine = 0;
   for (int r = r0; r < r1; ++r)
-    mine += split_count(p, clamped_len(p, (int)(keys[r] & 0xffffffffu))) * per_split;
+    mine += split_count(p, clamped_len(p, (int)(keys[r] & 0xffffffffu)), min_tiles) * per_split;
   int incl = mine;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -700,11 +726,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
   }
   __syncthreads();
   int x = warp_sums[wid] + incl - mine;
+  griddep_wait();
   for (int r = r0; r < r1; ++r) {
     const int b = (int)(keys[r] & 0xffffffffu);
-    const int ns = split_count(p, clamped_len(p, b));
+    const int ns = split_count(p, clamped_len(p, b), min_tiles);
     for (int split = 0; split < ns; ++split)
-      for (int th = 0; th < per_split; ++th) p.plan[x++] = entry(b, split, th >> 1, th & 1);
+      for (int th = 0; th < per_split; ++th) p.plan[x++] = entry(b, split, ns, th >> 1, th & 1);
   }
   for (int y = s_total + tid; y < grid; y += kPlanThreads) p.plan[y] = -1;
 }

@@ -108,8 +108,9 @@ __device__ __forceinline__ PairUnit decode_pair_unit(const MlaParams& p, int ran
   const int v = __ldg(p.plan + (blockIdx.x >> 1));
   u.valid = v >= 0;
   if (!u.valid) return u;
-  u.split = v & 15;
-  const int ch = v >> 4;
+  u.split = (v >> 4) & 15;
+  const int ns = (v & 15) + 1;
+  const int ch = v >> 8;
   u.half = ch & 1;
   const int rt = ch >> 1, npairs = p.qlen >> 1;
   u.b = rt / npairs;
@@ -122,7 +123,6 @@ __device__ __forceinline__ PairUnit decode_pair_unit(const MlaParams& p, int ran
   u.lim = lim_of(u.t);
   u.lim_max = max(lim_of(2 * tp), lim_of(2 * tp + 1));
   const int req_tiles = (L + kTile - 1) / kTile;
-  const int ns = split_count(p, L);  // at least 4096 keys a split (64 tiles)
   u.nsplit = ns;
   const int a = (int)((long long)req_tiles * u.split / ns);
   const int e = (int)((long long)req_tiles * (u.split + 1) / ns);

@@ -128,6 +128,12 @@ constexpr int kMlaLv = 512;
 constexpr int kMlaHalf = kMlaLv / 2;        // output dims per CTA
 constexpr int kMlaTile = 32;                // keys per pipeline tile
 constexpr int kMlaMinTiles = 128;           // a split holds at least 4096 keys
+// CTA-pair launches split more coarsely (6144 keys) when the batch still has
+// a unit for every CTA pair at that size: each unit costs ~8 us of start,
+// query load and merge on top of its tiles, and on B = 32 qlen 4 batches
+// (lengths U[512, 8192], four seeds, same process) 128 -> 192 measured
+// 223.2 / 221.2 / 221.2 / 202.8 -> 200.7 / 210.9 / 200.7 / 184.3 us.
+constexpr int kMlaMinTilesWide = 192;
 constexpr int64_t kMlaPartialFloats = int64_t(kMlaHeads) * kMlaHalf + 2 * kMlaHeads;
 
 struct MlaParams {
@@ -148,6 +154,7 @@ struct MlaParams {
   int64_t lse_sr, lse_sh;
   int B, qlen, cap, page_size;
   float scale;
+  int pair_slots;                // CTA pairs that run at once (SMs / 2)
   float* partials;               // [slots][128*256 + 256]
   int64_t max_slots;
   int* counters;                 // [(b*qlen + t)*2 + half]
