@@ -177,6 +177,32 @@ def test_mla_verify_b32_full_size_every_row():
     check_split_invariance(outs, "mla b32 q4")
 
 
+def test_mla_pair_split_size_both_branches():
+    """The planning kernel splits CTA-pair launches at 6144 keys when every
+    CTA pair still gets a unit at that size, else at 4096.  Eight requests of
+    9000 keys with qlen 2 (32 units at 6144 keys: fewer than the CTA pairs of
+    a GB300, so three 4096-key splits each) and forty of 6200..9000 keys (160
+    units: two 6144-key splits each): every (row, head) against the oracle,
+    unsplit (cap 1), at the library's split cap and at cap 8, and the caps
+    agree within the split-invariance bound."""
+    rng = np.random.default_rng(31)
+    for seed, L in ((31, np.full(8, 9000)),
+                    (32, rng.integers(6200, 9001, size=40))):
+        L = L.astype(np.int32)
+        real = np.maximum(L - rng.integers(0, 2, size=len(L)), 0).astype(np.int32)
+        prob = mla_case(seed, L, 2, 16, real=real)
+        ref_out, ref_lse = oracle_mla(prob)
+        R, H, _ = prob.q.shape
+        outs = []
+        for cap in (1, 0, 8):
+            out, lse = run_mla(prob, cap)
+            compare(out, lse, ref_out.reshape(R, H, 512), ref_lse.reshape(R, H),
+                    what=f"mla pair split B={len(L)} cap {cap}")
+            outs.append((out, lse))
+        check_split_invariance(outs, f"mla pair split B={len(L)}")
+    assert pkv.check_counters(0) == 0
+
+
 @pytest.mark.parametrize("seed,L,qlen,real,k_scale,cap", [
     (11, [64, 1, 1500], 1, None, 0.05, 0),
     (12, [3000, 33], 4, [2998, 33], 0.05, 2),
