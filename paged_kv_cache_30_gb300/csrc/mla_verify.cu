@@ -617,13 +617,17 @@ __global__ void __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 }
 
 // ------------------------------------------------------------ work plan --
-// One CTA writes every verify CTA's unit (see decode_unit) or -1.  The
-// units (split < the request's split count) come in order of decreasing
-// split size, i.e. tiles per split, ties by request index (beyond
-// kPlanSortMax requests: request order), so the CTAs that start last are the
-// short ones; a request's units are consecutive (split-major, then verify
-// token, then half: the CTAs that read the same keys run side by side); -1
-// fills the rest of the launch.
+// One CTA writes every verify CTA's unit (plan_entry: request, split and
+// split count, verify token -- or token pair for CTA-pair launches -- and
+// half) or -1.  The units (split < the request's split count) come in order
+// of decreasing split size, i.e. tiles per split, ties by request index
+// (beyond kPlanSortMax requests: request order), so the CTAs that start last
+// are the short ones; a request's units are consecutive (split-major, then
+// verify token, then half: the CTAs that read the same keys run side by
+// side); -1 fills the rest of the launch.  A split holds at least
+// kMlaMinTiles tiles, or kMlaMinTilesWide for CTA-pair launches whose batch
+// still has a unit for every CTA pair at that size: each unit costs ~8 us
+// beyond its tiles, so fewer, longer units win once the GPU is full.
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanSortMax = 8192;
 
