@@ -196,6 +196,46 @@ def oracle_baseline(layers, budget_s: float, threads: int):
     return done_bytes / t_used / 1e9, t_used, groups
 
 
+def oracle_single_thread(budget_s: float):
+    """The oracle on one host thread on the tiny GQA batch (whole calls) and on
+    the B = 32 qlen 4 MLA verify batch (whole (row, head) pairs of the longest
+    request, until ~budget_s of work): a reported baseline beside the all-core
+    figure."""
+    import numpy as np
+    import oracle
+    from paged_kv_cache_30_gb300 import workloads as W
+    tiny = W.tiny_gqa(0)
+    n, t_used = 0, 0.0
+    while t_used < budget_s or n < 3:
+        t = time.perf_counter()
+        oracle.gqa_decode(tiny.q, tiny.kv_cache, tiny.block_table, tiny.seq_lens, tiny.sinks,
+                          tiny.window, tiny.scale, tiny.page_size, nthreads=1)
+        t_used += time.perf_counter() - t
+        n += 1
+    res = {"tiny_gqa_b4": {"calls_per_s": n / t_used, "calls": n, "cores": 1}}
+    mla = W.mla_verify(0)
+    R, H, _ = mla.q.shape
+    b = int(np.argmax(mla.seq_lens.numpy()))
+    L = int(mla.seq_lens[b])
+    Lr = int(mla.real_seq_lens[b]) if mla.real_seq_lens is not None else L
+    flops, t_used, done = 0.0, 0.0, 0
+    pairs = np.arange(b * mla.qlen * H, (b + 1) * mla.qlen * H, dtype=np.int64)
+    while t_used < budget_s and done < len(pairs):
+        rows = pairs[done:done + 16]
+        t = time.perf_counter()
+        oracle.mla_verify(mla.q, mla.latent_cache, mla.block_table, mla.seq_lens,
+                          mla.real_seq_lens, mla.qlen, mla.scale, mla.page_size, rows=rows,
+                          nthreads=1)
+        t_used += time.perf_counter() - t
+        for x in rows:
+            tok = int(x) // H - b * mla.qlen
+            flops += 2.0 * max(min(L - mla.qlen + 1 + tok, Lr), 0) * (576 + 512)
+        done += len(rows)
+    res["mla_verify_b32_q4"] = {"GFLOP_per_s": flops / t_used / 1e9, "row_heads": done,
+                                "cores": 1}
+    return res
+
+
 # ---------------------------------------------------- the other workloads ---
 def mla_flops(prob) -> float:
     """Algorithmic MLA flops: every (row, head) attends lim keys with a 576-wide
@@ -706,6 +746,7 @@ def run_gpu(args, rank, world, local_rank):
                          f"{groups / (layers[0].q.shape[0] * layers[0].kv_cache.shape[1]):.1f} "
                          f"passes over the layer), {t_used:.1f} s of fp64 oracle work on "
                          f"{threads} threads"}
+        cpu["single_thread"] = oracle_single_thread(2.0)
 
     extra = None
     try:
