@@ -320,7 +320,8 @@ PKV_API int pkv_mla_verify_attn_fp8_native(const pkv_tensor* q8, const pkv_tenso
  * as num_kv_splits; with num_kv_splits == 0 the library picks its own cap, and
  * in either case each request's actual split count is chosen on the device
  * from the lengths (GQA: about four work items per CTA, at least 256 keys per
- * split; MLA: at least 4096 keys per split).
+ * split; MLA: at least 4096 keys per split, 6144 when two verify tokens share
+ * a CTA pair and the batch still gives every CTA pair a unit at that size).
  */
 PKV_API int pkv_num_kv_splits(int max_seq_len, int batch, int qlen, int num_heads, int sm_count,
                               int block_h, double occupancy, int min_work_per_split,

@@ -580,7 +580,8 @@ static int mla_verify_impl(const pkv_tensor* q, const pkv_tensor* q8, const pkv_
   if ((rc = workspace_for(dev, stream, &st, &capturing))) return rc;
   const pkv::Workspace& ws = st->ws;
   // splits: at most 16 per (request, token, half); the device uses fewer for
-  // short requests (at least 4096 keys per split)
+  // short requests (at least 4096 keys per split, or 6144 on CTA pairs when
+  // the batch is large enough: the planning kernel's choice)
   int64_t cap = num_kv_splits == 0 ? 16 : std::min<int64_t>(num_kv_splits, 16);
   // each slot: one partial plus one plan entry (the plan sits at the end)
   const int64_t max_slots = int64_t(ws.partial_bytes) / (pkv::kMlaPartialFloats * 4 + 4);
