@@ -81,6 +81,8 @@ def mla_case(seed, L, qlen, P=16, real=None, Lmax=None, has_real=True, cap=0, po
     (3, [4097, 1500], 4, 16, None, 1),
     (4, [3000, 3000], 3, 16, [2999, 10], 3),
     (5, [70, 64, 63], 4, 32, None, 16),
+    (6, [5000, 9, 700], 6, 16, [4998, 0, 700], 0),     # three token pairs, one request empty
+    (7, [2049, 8000], 8, 32, [2049, 7993], 4),         # four token pairs, page 32
 ])
 def test_mla_small_cases(seed, L, qlen, P, real, cap):
     prob = mla_case(seed, L, qlen, P, real=real, cap=cap)
