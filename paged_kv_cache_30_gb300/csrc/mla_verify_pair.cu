@@ -101,8 +101,8 @@ struct PairUnit {
   bool valid;
 };
 
-// The unit of this CTA's cluster from the plan (entry ((b * qlen / 2 + tp) *
-// 2 + half) * 16 + split, or -1), and this CTA's token 2tp + rank.
+// The unit of this CTA's cluster from the plan (plan_entry: request b, token
+// pair tp, half, split and split count; or -1), and this CTA's token 2tp + rank.
 __device__ __forceinline__ PairUnit decode_pair_unit(const MlaParams& p, int rank) {
   PairUnit u;
   const int v = __ldg(p.plan + (blockIdx.x >> 1));
