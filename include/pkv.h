@@ -400,6 +400,18 @@ PKV_API int pkv_mla_kv_append(const pkv_tensor* latent, const pkv_tensor* latent
 PKV_API int pkv_check_errors(int device, int32_t* flags);
 
 /*
+ * pkv_selftest_wait_timeout -- failure-detection self-test.  Launches, on
+ * `stream` of `device` (which must have a workspace: pkv_init), one CTA that
+ * waits on an mbarrier nothing ever arrives on, through the same bounded wait
+ * the attention kernels use.  The wait gives up after about 2^31 SM cycles
+ * (about a second), raises bit 4 of the device error word and the kernel
+ * returns: no fault, no hang, and the context stays usable.
+ * pkv_check_errors(device) then reports the bit.  Returns PKV_OK, or
+ * PKV_ERR_INVALID_ARG / PKV_ERR_CUDA.
+ */
+PKV_API int pkv_selftest_wait_timeout(int device, void* stream);
+
+/*
  * pkv_check_counters -- count the non-zero arrival counters and scheduler
  * words of `device` (synchronises the device).  The kernels reset every
  * counter they use before returning, so a non-zero count after a completed

@@ -95,11 +95,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.pkv_num_kv_splits.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_double, i32, i32]
         lib.pkv_check_errors.argtypes = [i32, ctypes.POINTER(ctypes.c_int32)]
         lib.pkv_check_counters.argtypes = [i32, ctypes.POINTER(ctypes.c_int64)]
+        lib.pkv_selftest_wait_timeout.argtypes = [i32, vp]
         lib.pkv_last_error.restype = ctypes.c_char_p
         for name in ("pkv_init", "pkv_paged_decode_attn", "pkv_paged_decode_attn_noalloc",
                      "pkv_mla_verify_attn", "pkv_mla_quantize_q",
                      "pkv_mla_verify_attn_fp8_native", "pkv_gqa_kv_append", "pkv_mla_kv_append",
                      "pkv_num_kv_splits", "pkv_check_errors", "pkv_check_counters",
+                     "pkv_selftest_wait_timeout",
                      "pkv_shutdown", "pkv_version"):
             getattr(lib, name).restype = i32
         if path is None:
@@ -259,6 +261,15 @@ def check_errors(device: int = 0) -> int:
     if rc < 0:
         raise PkvError(rc, last_error())
     return flags.value
+
+
+def selftest_wait_timeout(device: int = 0, stream=None) -> None:
+    """Failure-detection self-test (C: pkv_selftest_wait_timeout): a bounded
+    wait that runs out (~1 s) and raises bit 4 of the device error word."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    _check(load_library().pkv_selftest_wait_timeout(
+        device, ctypes.c_void_p(s if isinstance(s, int) else s.cuda_stream)))
 
 
 def check_counters(device: int = 0) -> int:

@@ -359,6 +359,21 @@ PKV_API int pkv_check_errors(int device, int32_t* flags) {
   return fail(PKV_ERR_CUDA, "device error word 0x%x", v);
 }
 
+PKV_API int pkv_selftest_wait_timeout(int device, void* stream_ptr) {
+  if (device < 0 || device >= kMaxDevices) return fail(PKV_ERR_INVALID_ARG, "device %d", device);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[device];
+  if (!st.ws.base) return fail(PKV_ERR_INVALID_ARG, "device %d has no workspace: call pkv_init", device);
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(device);
+  const cudaError_t e =
+      pkv::launch_wait_selftest(static_cast<int*>(st.ws.err), static_cast<cudaStream_t>(stream_ptr));
+  cudaSetDevice(prev);
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test launch");
+  return PKV_OK;
+}
+
 PKV_API int pkv_check_counters(int device, int64_t* nonzero) {
   if (!nonzero) return fail(PKV_ERR_INVALID_ARG, "nonzero is NULL");
   *nonzero = 0;

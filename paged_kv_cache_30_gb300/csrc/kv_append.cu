@@ -94,6 +94,27 @@ __global__ void __launch_bounds__(kWarps * 32) mla_kv_append_kernel(const Append
 
 }  // namespace
 
+// Failure-detection self-test: one CTA waits on an mbarrier that nothing ever
+// arrives on, through the bounded wait every kernel of the library uses; the
+// wait gives up after ~2^31 cycles, raises DEVERR_WAIT_TIMEOUT in `err` and the
+// kernel returns (no fault, no hang).
+__global__ void wait_selftest_kernel(int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(b, 0, err);
+  __syncthreads();
+}
+
+cudaError_t launch_wait_selftest(int* err, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gqa_kv_append(const AppendParams& p, cudaStream_t stream) {
   const long long rows = (long long)p.B * p.Hkv;
   const unsigned grid = (unsigned)((rows + kWarps - 1) / kWarps);

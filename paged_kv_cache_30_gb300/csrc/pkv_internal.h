@@ -216,6 +216,8 @@ struct AppendParams {
   int* err;
 };
 cudaError_t launch_gqa_kv_append(const AppendParams& p, cudaStream_t stream);
+// one CTA whose bounded mbarrier wait runs out and raises DEVERR_WAIT_TIMEOUT in err
+cudaError_t launch_wait_selftest(int* err, cudaStream_t stream);
 cudaError_t launch_mla_kv_append(const AppendParams& p, cudaStream_t stream);
 
 // Large dynamic shared memory is an attribute of a kernel on the current

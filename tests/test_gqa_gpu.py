@@ -288,6 +288,26 @@ def test_bad_block_table_entry_is_flagged_not_faulted(L):
     check(prob, what="after bad table")
 
 
+def test_bounded_wait_gives_up_and_reports_without_fault():
+    """Failure detection without a GPU fault: one CTA waits on an mbarrier that
+    nothing arrives on, through the kernels' bounded wait.  After about a
+    second the wait gives up, bit 4 of the device error word is raised and
+    pkv_check_errors reports it; the context stays usable (the next decode
+    matches the oracle)."""
+    import ctypes
+    lib = pkv.load_library()
+    flags = ctypes.c_int32(0)
+    lib.pkv_check_errors(0, ctypes.byref(flags))  # start from a clear word
+    pkv.selftest_wait_timeout(0)
+    torch.cuda.synchronize()
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.check_errors(0)
+    assert ei.value.code == -6 and "0x4" in str(ei.value)
+    assert pkv.check_errors(0) == 0  # read and cleared
+    check(W.gqa_problem(22, 3, 16, 2, 16, "uniform", 1, 900, sinks=True),
+          what="after a timed-out wait")
+
+
 @pytest.mark.parametrize("window, cap, maxb", [(0, 0, 4), (128, 0, 4), (0, 1, 4), (0, 0, 40),
                                                (0, 3, 40)])
 def test_seq_len_beyond_block_table_is_flagged(window, cap, maxb):
