@@ -205,14 +205,16 @@ def test_mla_pair_split_size_both_branches():
     assert pkv.check_counters(0) == 0
 
 
-@pytest.mark.parametrize("seed,L,qlen,real,k_scale,cap", [
-    (11, [64, 1, 1500], 1, None, 0.05, 0),
-    (12, [3000, 33], 4, [2998, 33], 0.05, 2),
-    (13, [700, 2049], 2, None, 0.125, 16),
+@pytest.mark.parametrize("seed,L,qlen,real,k_scale,cap,P", [
+    (11, [64, 1, 1500], 1, None, 0.05, 0, 16),
+    (12, [3000, 33], 4, [2998, 33], 0.05, 2, 16),
+    (13, [700, 2049], 2, None, 0.125, 16, 16),
+    (14, [2000, 65, 31], 3, [1999, 65, 31], 0.05, 0, 32),   # 32-token pages: two boxes a page
+    (15, [5000, 1], 1, None, 0.02, 4, 32),
 ])
-def test_mla_fp8_small_cases(seed, L, qlen, real, k_scale, cap):
+def test_mla_fp8_small_cases(seed, L, qlen, real, k_scale, cap, P):
     L = np.asarray(L, dtype=np.int32)
-    prob = W.mla_problem(seed, B=len(L), qlen=qlen, H=128, page_size=16, lengths="const",
+    prob = W.mla_problem(seed, B=len(L), qlen=qlen, H=128, page_size=P, lengths="const",
                          Lmin=1, Lmax=int(L.max()), seq_lens=L, fp8=True, k_scale=k_scale,
                          has_real=real is not None, num_kv_splits=cap)
     if real is not None:
