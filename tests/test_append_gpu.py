@@ -72,7 +72,7 @@ def test_gqa_append_bad_entries_are_flagged_and_not_written():
 
 
 @pytest.mark.parametrize("fp8,qlen,P", [(False, 1, 16), (False, 4, 32), (True, 1, 16),
-                                        (True, 4, 16)])
+                                        (True, 4, 16), (True, 3, 32)])
 def test_mla_append_matches_oracle_bytewise(fp8, qlen, P):
     L = np.array([4, 17, 33, 64, 2, 500], dtype=np.int32)
     prob = W.mla_problem(20 + qlen, B=len(L), qlen=qlen, H=128, page_size=P, lengths="const",
